@@ -35,7 +35,6 @@ def test_permutation_is_a_permutation():
 def test_config_structures():
     c1, pg = W.config1()
     assert c1.q.dtype == torch.float32 and tuple(c1.q.shape) == (2, 64, 4, 64)
-    assert sorted(pg["block_table"].reshape(-1).tolist()) != list(range(8)) or True
     assert len(set(pg["block_table"].reshape(-1).tolist())) == 8
     ctx = W.config3_lengths()
     assert ctx.min() >= 128 and ctx.max() <= 4096 and len(ctx) == 64
@@ -44,7 +43,7 @@ def test_config_structures():
     p = W.paged_case(3, [30, 0, 17], [2, 5, 16], 4, 2, 8, num_blocks=10, max_blocks_per_seq=4)
     bt = p.block_table.numpy()
     used = [b for s in range(3) for b in bt[s] if b >= 0]
-    assert len(used) == len(set(used)) == 3 + 1 + 3
+    assert len(used) == len(set(used)) == 2 + 1 + 3  # ceil(32/16) + ceil(5/16) + ceil(33/16)
     assert p.slot_mapping.shape[0] == 23 and p.total_q == 23
     # slots land inside the owning sequence's blocks at positions ctx_old .. ctx-1
     sm = p.slot_mapping.tolist()
