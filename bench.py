@@ -1,0 +1,429 @@
+"""Benchmark of libfattn on one GB300 (or N independent replicas under torchrun).
+
+Primary line: config 2, causal prefill B=4 T=2048 Hq=12 Hkv=2 d=128 (bf16
+inputs, fp32 accumulation) -> algorithmic TFLOP/s (4*d per unmasked
+query/key pair).  Secondary entries: config 3 paged decode (KV GB/s),
+config 4 long masked prefill, config 5 chunked prefill over the paged cache.
+
+Timing: W warm-up steps, then exactly K timed steps; each step's kernel work
+is bracketed by CUDA events on the launching stream and the L2 cache is
+flushed (a 2x-L2-sized buffer is overwritten) before every step, outside the
+events.  Barrier + synchronize on both sides of the timed region; the max over
+ranks is taken.  `e2e` repeats the primary step through the same C-ABI with
+the inputs in pinned host memory: host->device copies of q/k/v, the call and
+the device->host copy of the output are all inside the timed region.
+
+`--impl reference` times the fp64 CPU oracle (the only other implementation
+of this method here) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "prefill attn TFLOP/s & paged-decode KV GB/s on 1 GB300, % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profile_traffic():
+    """Per-launch DRAM bytes from committed ncu summaries (lines 'traffic <kernel-key> <bytes>')."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if os.path.exists(path):
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 3 and parts[0] == "traffic":
+                    out[parts[1]] = float(parts[2])
+    return out
+
+
+# ------------------------------------------------------------ distributed ---
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, ws: int) -> float:
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ timing ---
+class Timer:
+    """Per-step CUDA-event timing on the current stream with an L2 flush before each step."""
+
+    def __init__(self, flush_bytes: int):
+        self.flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda")
+
+    def run(self, step, steps: int, warmup: int, ws: int, sampler: ClockSampler | None = None,
+            min_warm_s: float = 0.0):
+        from paged_kv_cache_tiled_gb300 import fattn as F
+        t0 = time.time()
+        i = 0
+        while i < warmup or (time.time() - t0) < min_warm_s:
+            self.flush.fill_(float(i))
+            step()
+            i += 1
+        torch.cuda.synchronize()
+        if F.fa_get_error() != F.FA_OK:
+            raise RuntimeError("device error during warm-up")
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        launches = 0
+        barrier(ws)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(steps):
+            self.flush.fill_(float(i))
+            starts[i].record()
+            step()
+            ends[i].record()
+            launches += F.fa_last_launch_count()
+        torch.cuda.synchronize()
+        barrier(ws)
+        wall = time.perf_counter() - wall0
+        if F.fa_get_error() != F.FA_OK:
+            raise RuntimeError("device error during timed steps")
+        times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return float(np.mean(times)), launches, wall, times
+
+
+# ---------------------------------------------------------------- workloads ---
+def prefill_setup(case):
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    out = torch.empty_like(q)
+    return q, k, v, out
+
+
+def bench_prefill(F, timer, case, steps, warmup, ws, peaks, sampler=None, masked=False, min_warm_s=0.0):
+    q, k, v, out = prefill_setup(case)
+    flops = W.attention_flops(case.T, case.T, case.d, case.B * case.Hq, True)
+    if masked:
+        M = case.mask.cuda()
+        wsb = torch.empty(F.fa_prefill_masked_workspace_size(case.T), dtype=torch.uint8, device="cuda")
+
+        def step():
+            F.fa_prefill_masked(q, k, v, M, causal=False, scale=case.scale, out=out, ws=wsb)
+    else:
+        def step():
+            F.fa_prefill(q, k, v, causal=case.causal, scale=case.scale, out=out)
+    if sampler:
+        sampler.start()
+    ms, launches, wall, _ = timer.run(step, steps, warmup, ws, min_warm_s=min_warm_s)
+    clocks = sampler.stop() if sampler else None
+    ms = reduce_max(ms, ws)
+    tflops = flops / (ms * 1e-3) / 1e12
+    return dict(ms=ms, tflops=tflops, flops=flops, launches=launches, clocks=clocks, wall=wall,
+                tensors=(q, k, v, out), step=step)
+
+
+def paged_setup(F, p):
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    F.fa_cache_append(p.k_new.cuda(), p.v_new.cuda(), kc, vc, p.slot_mapping.cuda())
+    torch.cuda.synchronize()
+    return dict(q=p.q.cuda(), kc=kc, vc=vc, bt=p.block_table.cuda(), ctx=p.ctx_lens.cuda(), ql=p.q_lens.cuda(),
+                out=torch.empty(p.total_q, p.Hq, p.d, dtype=torch.bfloat16, device="cuda"),
+                ws=torch.empty(F.fa_paged_attn_workspace_size(p.num_seqs, p.max_blocks_per_seq, p.Hq, p.Hkv, p.d,
+                                                              p.total_q), dtype=torch.uint8, device="cuda"))
+
+
+def paged_bytes(p):
+    """Algorithmic bytes: every cached K/V element of every context read once
+    (per kv head), queries read once, outputs written once, block-table
+    entries and lengths read once."""
+    ctx = p.ctx_lens.numpy().astype(np.int64)
+    kv = int(ctx.sum()) * p.Hkv * p.d * 2 * 2
+    qo = 2 * p.total_q * p.Hq * p.d * 2
+    tables = int(((ctx + 15) // 16).sum()) * 4 + 8 * p.num_seqs
+    return kv + qo + tables, kv
+
+
+def paged_flops(p):
+    ctx = p.ctx_lens.numpy().astype(np.int64)
+    ql = p.q_lens.numpy().astype(np.int64)
+    tot = 0.0
+    for c, q in zip(ctx, ql):
+        tot += W.attention_flops(int(q), int(c), p.d, p.Hq, p.causal)
+    return tot
+
+
+def bench_paged(F, timer, p, steps, warmup, ws, with_append=False):
+    t = paged_setup(F, p)
+    max_q = int(p.q_lens.max())
+    if with_append:
+        kn, vn, sm = p.k_new.cuda(), p.v_new.cuda(), p.slot_mapping.cuda()
+
+    def step():
+        if with_append:
+            F.fa_cache_append(kn, vn, t["kc"], t["vc"], sm)
+        F.fa_paged_attn(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["ql"], causal=p.causal, scale=p.scale,
+                        out=t["out"], max_q_len=max_q, ws=t["ws"])
+    ms, launches, wall, _ = timer.run(step, steps, warmup, ws)
+    ms = reduce_max(ms, ws)
+    return dict(ms=ms, launches=launches, wall=wall)
+
+
+# ----------------------------------------------------------- cpu baseline ---
+def oracle_sample_c2(batches: int = 1):
+    """Bounded sample of config 2 for the CPU oracle: the first `batches`
+    batch entries, all 12 heads, full T=2048 causal."""
+    case = W.config2()
+    q, k, v = case.q[:batches].contiguous(), case.k[:batches].contiguous(), case.v[:batches].contiguous()
+    flops = W.attention_flops(case.T, case.T, case.d, batches * case.Hq, True)
+    return case, q, k, v, flops
+
+
+def time_oracle(q, k, v, case, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, True, case.scale, nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(batches=1):
+    case, q, k, v, flops = oracle_sample_c2(batches)
+    threads = os.cpu_count() or 1
+    dt = time_oracle(q, k, v, case, threads)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"config 2 rows of batch entries 0..{batches - 1} (all 12 heads, T=2048, causal): "
+                      f"{flops / 1e9:.2f} GFLOP algorithmic in {dt:.2f} s on {threads} threads"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    case, q, k, v, flops = oracle_sample_c2(1)
+    threads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        time_oracle(q, k, v, case, threads)
+    times = [time_oracle(q, k, v, case, threads) for _ in range(args.steps)]
+    ms = float(np.mean(times)) * 1e3
+    val = flops / (ms * 1e-3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "config 2 causal prefill B=4 T=2048 Hq=12 Hkv=2 d=128; each step = batch entry 0 "
+                                   "(1/4 of the workload) through the fp64 CPU oracle"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": "batch entry 0 of config 2 per step"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- main ---
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    torch.cuda.set_device(local)
+    from paged_kv_cache_tiled_gb300 import build
+    build.build()
+    from paged_kv_cache_tiled_gb300 import fattn as F
+
+    peaks, peak_src = load_peaks()
+    traffic = profile_traffic()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    timer = Timer(max(2 * l2, 256 << 20))
+    sampler = ClockSampler(local)
+
+    # ---------------- primary: config 2 prefill
+    c2 = W.config2()
+    res = bench_prefill(F, timer, c2, args.steps, args.warmup, ws, peaks, sampler=sampler, min_warm_s=1.5)
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roof = {"bound": "tensor", "achieved": res["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": res["tflops"] / tc_peak, "traffic": traffic.get("attn_tc_dense_c2"),
+            "kernel": "attn_tc_kernel<128, dense>", "peak_source": f"{peak_src} bf16 burst",
+            "algorithmic_flops_per_launch": res["flops"]}
+
+    # ---------------- e2e through host buffers
+    q, k, v, out = res["tensors"]
+    hq, hk, hv = (t.cpu().pin_memory() for t in (c2.q, c2.k, c2.v))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        F.fa_prefill(q, k, v, causal=True, scale=c2.scale, out=out)
+        hout.copy_(out, non_blocking=True)
+    e_ms, _, _, _ = timer.run(e2e_step, args.steps, args.warmup, ws)
+    e_ms = reduce_max(e_ms, ws)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size()
+    e2e = {"value": res["flops"] / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    line = {"metric": METRIC, "value": res["tflops"] * ws, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1) bf16 inputs with the shapes of config 2 (no weights needed)",
+            "config": {"workload": "config 2: causal prefill B=4 T=2048 Hq=12 Hkv=2 d=128 bf16, scale 1/sqrt(128)",
+                       "l2": "flushed before every timed step (2x L2 buffer overwrite, outside the events)",
+                       "replicas": ws},
+            "roofline": roof, "e2e": e2e, "gpu_launches": res["launches"], "clocks": res["clocks"]}
+
+    # ---------------- secondary workloads
+    if not args.no_secondary:
+        sec = []
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        # config 3: paged decode
+        c3 = W.config3()
+        r3 = bench_paged(F, timer, c3, args.steps, args.warmup, ws)
+        b3, kv3 = paged_bytes(c3)
+        gbs = b3 / (r3["ms"] * 1e-3) / 1e9
+        sec.append({"workload": "config 3: paged decode, 64 seqs ctx U[128,4096], Hq=12 Hkv=2 d=128, 16-token blocks",
+                    "metric": "paged-decode KV GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": r3["ms"],
+                    "kv_bytes": kv3, "algorithmic_bytes": b3, "gpu_launches": r3["launches"],
+                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                                 "traffic": traffic.get("paged_decode_c3"), "peak_source": f"{peak_src} hbm copy",
+                                 "kernel": "paged_decode_kernel<128> + paged_merge_kernel<128>"}})
+        del c3
+        # config 4: long masked prefill (and the same problem through the causal flag)
+        steps4 = max(3, min(args.steps, 10))
+        c4 = W.config4()
+        r4 = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks, masked=True)
+        r4c = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks)
+        for r, name in ((r4, "additive mask M (-inf above diagonal) via fa_prefill_masked"),
+                        (r4c, "causal flag via fa_prefill")):
+            sec.append({"workload": f"config 4: long prefill B=1 T=16384 Hq=32 Hkv=8 d=128, {name}",
+                        "metric": "prefill attn TFLOP/s", "value": r["tflops"], "unit": "TFLOP/s",
+                        "ms_per_step": r["ms"], "gpu_launches": r["launches"],
+                        "roofline": {"bound": "tensor", "achieved": r["tflops"],
+                                     "peak": float(peaks.get("bf16_tflops_sustained", tc_peak)), "unit": "TFLOP/s",
+                                     "frac": r["tflops"] / float(peaks.get("bf16_tflops_sustained", tc_peak)),
+                                     "traffic": None, "peak_source": f"{peak_src} bf16 sustained"}})
+        del c4, r4, r4c
+        torch.cuda.empty_cache()
+        # config 5: append + chunked prefill over the paged cache
+        c5 = W.config5()
+        r5 = bench_paged(F, timer, c5, args.steps, args.warmup, ws, with_append=True)
+        f5 = paged_flops(c5)
+        b5, kv5 = paged_bytes(c5)
+        tf5 = f5 / (r5["ms"] * 1e-3) / 1e12
+        t_bound = max(f5 / (tc_peak * 1e12), b5 / (hbm * 1e9))
+        sec.append({"workload": "config 5: append + chunked prefill, 16 seqs ctx U[0,8192] + chunk U[1,512], "
+                                "Hq=32 Hkv=8 d=128",
+                    "metric": "prefill attn TFLOP/s", "value": tf5, "unit": "TFLOP/s", "ms_per_step": r5["ms"],
+                    "gpu_launches": r5["launches"], "algorithmic_flops": f5, "algorithmic_bytes": b5,
+                    "roofline": {"bound": "tensor" if f5 / (tc_peak * 1e12) > b5 / (hbm * 1e9) else "hbm",
+                                 "achieved": tf5, "peak": tc_peak, "unit": "TFLOP/s",
+                                 "frac": t_bound / (r5["ms"] * 1e-3), "traffic": None,
+                                 "note": "frac = max(F/P_tc, B/BW) / measured time"}})
+        line["secondary"] = sec
+
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(1)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

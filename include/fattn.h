@@ -1,0 +1,199 @@
+/*
+ * libfattn -- exact tiled attention, paged attention and the fused KV-cache
+ * append for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operations follow "Fast Attention Kernels and Operator Fusion":
+ *   - section "FlashAttention-Style Kernels", attention equation
+ *       Attention(Q, K, V) = softmax(Q K^T / sqrt(d) + M) V,
+ *     computed tile by tile with running softmax statistics so the T x T score
+ *     matrix never reaches device memory (same section, the paragraph on
+ *     processing queries, keys and values in tiles);
+ *   - section "Paged Attention Kernels": keys and values stored in fixed
+ *     16-token blocks, a per-sequence block table translating logical block
+ *     numbers to physical ones (the section's example maps logical blocks
+ *     0 1 2 3 to physical 17 4 29 8), and a kernel that reads every key and
+ *     value through that table;
+ *   - section "Operator Fusion", fusion list item on updating the KV cache
+ *     while transforming key and value tensors (the fused append).
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise.  The
+ *     caller owns all buffers, including workspaces; the library allocates no
+ *     device memory in any call.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream); they do
+ *     not synchronise the host.  Errors found on the device (a block-table
+ *     entry outside the pool, a slot outside the cache, an inconsistent length,
+ *     a bounded wait that expired) are recorded in a per-device error word and
+ *     read with fa_get_error().
+ *   - bf16 tensors are IEEE bfloat16 stored as 16-bit words.  Accumulation is
+ *     fp32; outputs are bf16 rounded to nearest even.
+ *   - Grouped-query attention: query head h reads kv head h / (Hq / Hkv).
+ *   - Causal masking with Tq <= Tk is bottom-right aligned: query i sits at
+ *     position i + Tk - Tq and sees keys j <= i + Tk - Tq.
+ *   - A query row that sees no key at all produces output 0 and LSE -inf.
+ *   - Supported: head dim d in {64, 128}; block_size 16; Hq % Hkv == 0;
+ *     sm_103a devices.  Anything else returns FA_ERR_UNSUPPORTED before any
+ *     launch; malformed arguments return FA_ERR_INVALID_ARG.  No call falls
+ *     back to the CPU.
+ */
+#ifndef FATTN_H
+#define FATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned buffer */
+    FA_ERR_UNSUPPORTED = 2, /* head dim, block size, GQA ratio or device not supported */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+    FA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (read by fa_get_error) */
+    FA_ERR_BOUNDS = 5,      /* device-side index check failed (read by fa_get_error) */
+    FA_ERR_WORKSPACE = 6    /* workspace missing or smaller than the size query says */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* fa_status_string(fa_status status);
+
+/*
+ * fa_prefill -- contiguous attention over [B, T, H, d] tensors.
+ * Passage: "FlashAttention-Style Kernels" (attention equation with M = 0, or
+ * the causal mask when `causal` != 0; tile-by-tile processing).
+ *   q   bf16 [B, T, Hq, d] row-major, 16-byte aligned
+ *   k,v bf16 [B, T, Hkv, d]
+ *   out bf16 [B, T, Hq, d] (written; may not alias the inputs)
+ *   lse fp32 [B, Hq, T] natural-log log-sum-exp of each row's scores, or NULL
+ *   scale multiplies Q K^T (1/sqrt(d) for the textbook form)
+ * Tq = Tk = T.  T may be any positive length (ragged final tile).
+ */
+fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int B, int T,
+                     int Hq, int Hkv, int d, int causal, float scale, float* lse,
+                     fa_stream_t stream);
+
+/*
+ * fa_prefill_masked -- as fa_prefill plus an additive mask M.
+ * Passage: "FlashAttention-Style Kernels", attention equation with additive M.
+ *   mask fp32 [T, T] row-major, broadcast over batch and heads; -inf allowed.
+ *        Added to the causal mask when `causal` != 0.
+ *   ws   device workspace of at least fa_prefill_masked_workspace_size(T)
+ *        bytes; holds the per-tile mask classes (all -inf: tile skipped; all
+ *        zero: mask not read; otherwise mask read and added) and the tile
+ *        order.  Contents need not be initialised.
+ */
+size_t fa_prefill_masked_workspace_size(int T);
+fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const float* mask,
+                            void* out, int B, int T, int Hq, int Hkv, int d, int causal,
+                            float scale, float* lse, void* ws, size_t ws_bytes,
+                            fa_stream_t stream);
+
+/*
+ * fa_stage_bf16 -- fp32 -> bf16 conversion, round to nearest even.  Used to
+ * stage fp32 q/k/v for the bf16 attention kernels.
+ *   src fp32 [n], dst bf16 [n]; both 16-byte aligned.
+ */
+fa_status fa_stage_bf16(const float* src, void* dst, size_t n, fa_stream_t stream);
+
+/*
+ * fa_cache_append -- fused write of new keys and values into the paged cache.
+ * Passage: "Operator Fusion", fusion list (updating the KV cache while
+ * transforming key and value tensors); "Paged Attention Kernels" (block
+ * storage).
+ *   k, v         [N, Hkv, d] in `in_dtype` (fp32 inputs are rounded to bf16, RNE)
+ *   k_cache, v_cache bf16 [num_blocks, Hkv, 16, d]
+ *   slot_mapping int32 [N]: token i goes to slot s = slot_mapping[i], i.e.
+ *                block s / 16, offset s % 16.  s < 0 skips the token;
+ *                s >= num_blocks * 16 sets FA_ERR_BOUNDS and skips it.
+ * Exact: bf16 inputs are copied bit for bit.
+ */
+fa_status fa_cache_append(const void* k, const void* v, void* k_cache, void* v_cache,
+                          const int32_t* slot_mapping, int N, int Hkv, int d, int num_blocks,
+                          fa_dtype in_dtype, fa_stream_t stream);
+
+/*
+ * fa_paged_attn -- attention of packed queries against the paged cache.
+ * Passage: "Paged Attention Kernels" (logical positions translated through
+ * the block table; 16-token blocks); "FlashAttention-Style Kernels" (the
+ * attention it computes; prefill processes many queries, decode one or a few
+ * while reading the growing cache).
+ *   q            bf16 [total_q, Hq, d], sequences packed in order
+ *   k_cache, v_cache bf16 [num_blocks, Hkv, 16, d]
+ *   block_table  int32 [num_seqs, max_blocks_per_seq]; entries past
+ *                ceil(ctx_lens[s] / 16) are never read
+ *   ctx_lens     int32 [num_seqs]: tokens of sequence s in the cache, the new
+ *                chunk included (its queries sit at ctx - q_len .. ctx - 1)
+ *   q_lens       int32 [num_seqs], 0 <= q_lens[s] <= ctx_lens[s];
+ *                sum(q_lens) must equal total_q
+ *   out          bf16 [total_q, Hq, d]
+ *   max_q_len    host-side upper bound on every q_lens[s] (total_q is always
+ *                a valid bound); used only to skip launching a kernel that
+ *                would find no work
+ *   block_size   must be 16
+ *   ws           workspace of at least fa_paged_attn_workspace_size(...) bytes
+ *                (split partials and scheduling lists); contents need not be
+ *                initialised
+ * Sequences whose (Hq/Hkv) * q_len <= 16 take the bandwidth-bound split-KV
+ * decode kernel followed by a log-sum-exp merge; longer chunks take the
+ * tensor-core kernel.  Both read K/V only through the block table.
+ */
+size_t fa_paged_attn_workspace_size(int num_seqs, int max_blocks_per_seq, int Hq, int Hkv, int d,
+                                    int total_q);
+fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_table, const int32_t* ctx_lens,
+                        const int32_t* q_lens, void* out, int num_seqs, int max_blocks_per_seq,
+                        int num_blocks, int Hq, int Hkv, int d, int block_size, int causal,
+                        float scale, int total_q, int max_q_len, void* ws, size_t ws_bytes,
+                        fa_stream_t stream);
+
+/*
+ * fa_get_error -- synchronises `stream`, then returns and clears the current
+ * device's error word: FA_OK, FA_ERR_BOUNDS or FA_ERR_TIMEOUT (FA_ERR_BOUNDS
+ * when both were recorded), or FA_ERR_CUDA if synchronisation itself failed.
+ */
+fa_status fa_get_error(fa_stream_t stream);
+
+/*
+ * fa_debug_gather_kv -- test hook for the block-table translation alone.
+ * Passage: "Paged Attention Kernels" (translate logical positions through
+ * the block table).  Writes out[s][t][h][:] = cache[block_table[s][t/16]][h][t%16][:]
+ * for t < ctx_lens[s]; positions t >= ctx_lens[s] are left untouched.
+ *   cache bf16 [num_blocks, Hkv, 16, d]; out bf16 [num_seqs, max_ctx, Hkv, d]
+ */
+fa_status fa_debug_gather_kv(const void* cache, const int32_t* block_table,
+                             const int32_t* ctx_lens, void* out, int num_seqs,
+                             int max_blocks_per_seq, int num_blocks, int Hkv, int d, int max_ctx,
+                             fa_stream_t stream);
+
+/*
+ * fa_debug_set_wait_limit -- bound, in nanoseconds, on every device-side
+ * pipeline wait of later launches (default 4e9).  A wait that runs out sets
+ * FA_ERR_TIMEOUT and the kernel exits cleanly.  Host-side setting; not
+ * synchronised with launches already queued.
+ */
+void fa_debug_set_wait_limit(unsigned long long nanoseconds);
+
+/*
+ * fa_debug_force_timeout -- test hook for failure detection.  While enabled,
+ * every pipelined kernel launched afterwards begins each of its roles with a
+ * wait on a barrier that nothing ever arrives on; the wait runs out after the
+ * current wait limit, the kernel records FA_ERR_TIMEOUT, drains the copies it
+ * issued, releases its tensor memory and exits.  No fault, trap or hang is
+ * involved.  Host-side setting.
+ */
+void fa_debug_force_timeout(int enable);
+
+/* Number of kernels the last successful call on this host thread launched. */
+int fa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H */

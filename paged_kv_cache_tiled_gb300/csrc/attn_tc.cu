@@ -1,0 +1,826 @@
+// Tensor-core attention for sm_103a: the tiled online-softmax algorithm of
+// "Fast Attention Kernels and Operator Fusion", section "FlashAttention-Style
+// Kernels" (queries, keys and values processed in tiles; per tile a block of
+// scores, an update of the softmax statistics and an on-chip accumulation of
+// the output; the score matrix never stored in device memory), for
+//   * contiguous prefill        (MODE_DENSE),
+//   * prefill with an additive mask M, classified per 128x128 tile beforehand
+//                               (MODE_MASKED),
+//   * chunked prefill over the paged cache, every K/V tile gathered block by
+//     block through the block table (MODE_PAGED; section "Paged Attention
+//     Kernels").
+//
+// CTA layout (320 threads, one CTA per SM, persistent over work units):
+//   warps 0-3   softmax warpgroup of Q slot 0, warps 4-7 of Q slot 1: thread
+//               r owns query row r of its slot (TMEM lane r; warp w may only
+//               touch TMEM lanes 32*(w%4) .. 32*(w%4)+31);
+//   warp 8      TMA producer: Q tiles once per unit, then K_j, V_j into a ring
+//               of shared-memory stages (128-byte swizzle);
+//   warp 9      tcgen05.mma issuer (one thread) and TMEM owner.
+// A work unit is two 128-row Q tiles ("slots") that share one kv head: two
+// query heads of the same GQA group over the same rows when Hq/Hkv is even,
+// otherwise two consecutive row tiles of one head.  Both slots consume the
+// same K/V tiles, so K/V are staged once for two Q tiles.
+//
+// TMEM (512 columns x 128 lanes, fp32): S0 [0,128), S1 [128,256),
+// O0 [256, 256+d), O1 [256+d, 256+2d).  P (bf16, packed two per column) is
+// written by the softmax threads over the first 64 columns of S and fed to
+// the P*V MMA straight from TMEM.
+//
+// MMA order per KV tile j:  PV0(j-1), QK0(j), PV1(j-1), QK1(j).  Each
+// tcgen05.commit tracks every MMA issued before it, so when slot s sees S_s(j)
+// complete, PV_s(j-1) is complete too and O_s may be rescaled.
+//
+// Softmax: base-2 exponentials with scale*log2(e) folded in; the running max
+// is only moved when a row's max grows by more than 8 (a factor 256), so O and
+// the row sum stay consistent with a possibly stale max (exact up to
+// rounding); P is rounded to bf16 for the tensor core, row sums stay fp32.
+#include <algorithm>
+
+#include "host_common.cuh"
+
+namespace fa {
+
+enum { MODE_DENSE = 0, MODE_MASKED = 1, MODE_PAGED = 2 };
+constexpr int kTcThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kTcRows = 128;  // rows of a Q tile and of a KV tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct TcCfg {
+    static constexpr int kAtoms = D / 64;                 // 128-byte column blocks per row
+    static constexpr int kAtomBytes = kTcRows * 128;      // one 128-row x 64-channel box
+    static constexpr int kTileBytes = kAtoms * kAtomBytes;
+    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kQBytes = 2 * kTileBytes;
+    static constexpr int kRingBytes = kStages * kTileBytes;
+    static constexpr int kNumBars = 2 * kStages + 2 * 5 + 2;
+    static constexpr int kSmem = 1024 + kQBytes + kRingBytes + kNumBars * 8 + 16;
+    static constexpr uint32_t kS0 = 0, kS1 = 128, kO0 = 256, kO1 = 256 + D;
+};
+
+struct TcParams {
+    int B, T;        // dense / masked: Tq = Tk = T
+    int Hq, Hkv, g;
+    int causal;
+    float scale_log2;
+    int pair_heads;  // 1: slots = heads (2pp, 2pp+1) of a group; 0: row tiles (2t, 2t+1) of one head
+    int num_units;   // dense / masked
+    uint16_t* out;
+    float* lse;
+    // masked
+    const float* mask;
+    const uint8_t* cls;
+    const int32_t* qt_order;
+    // paged
+    const int32_t* bt;
+    const int32_t* ctx_lens;
+    const int32_t* q_lens;
+    const int32_t* q_start;
+    const int32_t* work_list;
+    const int32_t* work_count;
+    int mbps, num_blocks;
+    DevCtx ctx;
+};
+
+struct Unit {
+    int b;          // batch (dense) / sequence (paged)
+    int hk;         // kv head
+    int head[2];    // query head per slot
+    int row0[2];    // first query row per slot (within T, or within the chunk)
+    int nrows[2];   // valid rows per slot (0: slot idle)
+    int qtok[2];    // row coordinate for the Q tile load
+    int kv_len;     // keys of the sequence (T or ctx)
+    int pos_off;    // key position of query row i is i + pos_off
+    int n_kt;       // KV tiles to scan
+};
+
+// i-th unit of this CTA: units are ordered longest first and dealt to the CTAs
+// in boustrophedon order (round i goes left to right when even, right to left
+// when odd), which evens out the per-CTA totals.
+__device__ __forceinline__ int unit_of(int i, int G) {
+    const int c = blockIdx.x;
+    return i * G + ((i & 1) ? (G - 1 - c) : c);
+}
+
+template <int MODE>
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+    Unit U;
+    if constexpr (MODE == MODE_PAGED) {
+        const int per_entry = p.pair_heads ? p.Hkv * (p.g / 2) : p.Hq;
+        const int e = u / per_entry, rest = u % per_entry;
+        const int seq = __ldg(p.work_list + 2 * e), t = __ldg(p.work_list + 2 * e + 1);
+        const int ql = __ldg(p.q_lens + seq), cl = __ldg(p.ctx_lens + seq), qs = __ldg(p.q_start + seq);
+        U.b = seq;
+        if (p.pair_heads) {
+            const int pp = rest % (p.g / 2);
+            U.hk = rest / (p.g / 2);
+            U.head[0] = U.hk * p.g + 2 * pp;
+            U.head[1] = U.head[0] + 1;
+            U.row0[0] = U.row0[1] = t * kTcRows;
+        } else {
+            U.head[0] = U.head[1] = rest;
+            U.hk = rest / p.g;
+            U.row0[0] = t * kTcRows;
+            U.row0[1] = (t + 1) * kTcRows;
+        }
+        int last = 0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            U.nrows[s] = max(0, min(kTcRows, ql - U.row0[s]));
+            U.qtok[s] = qs + U.row0[s];
+            if (U.nrows[s] > 0) last = max(last, U.row0[s] + U.nrows[s]);
+        }
+        U.kv_len = cl;
+        U.pos_off = cl - ql;
+        const int kv_end = p.causal ? min(cl, cl - ql + last) : cl;
+        U.n_kt = (kv_end + kTcRows - 1) / kTcRows;
+    } else {
+        const int nqt = (p.T + kTcRows - 1) / kTcRows;
+        if (p.pair_heads) {
+            const int half = p.g / 2;
+            const int upt = p.B * p.Hkv * half;
+            const int rank = u / upt, rest = u % upt;
+            int qt;
+            if constexpr (MODE == MODE_MASKED)
+                qt = __ldg(p.qt_order + rank);
+            else
+                qt = p.causal ? nqt - 1 - rank : rank;
+            U.b = rest / (p.Hkv * half);
+            U.hk = (rest / half) % p.Hkv;
+            const int pp = rest % half;
+            U.head[0] = U.hk * p.g + 2 * pp;
+            U.head[1] = U.head[0] + 1;
+            U.row0[0] = U.row0[1] = qt * kTcRows;
+        } else {
+            const int ntp = (nqt + 1) / 2;
+            const int upt = p.B * p.Hq;
+            const int rank = u / upt, rest = u % upt;
+            const int pt = (p.causal && MODE == MODE_DENSE) ? ntp - 1 - rank : rank;
+            U.b = rest / p.Hq;
+            U.head[0] = U.head[1] = rest % p.Hq;
+            U.hk = U.head[0] / p.g;
+            U.row0[0] = 2 * pt * kTcRows;
+            U.row0[1] = (2 * pt + 1) * kTcRows;
+        }
+        int last = 0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            U.nrows[s] = max(0, min(kTcRows, p.T - U.row0[s]));
+            U.qtok[s] = U.row0[s];
+            if (U.nrows[s] > 0) last = max(last, U.row0[s] + U.nrows[s]);
+        }
+        U.kv_len = p.T;
+        U.pos_off = 0;
+        const int kv_end = p.causal ? last : p.T;
+        U.n_kt = (kv_end + kTcRows - 1) / kTcRows;
+    }
+    return U;
+}
+
+// Mask class of (query tile of slot s, KV tile kt): 0 skip, 1 no mask, 2 mixed.
+template <int MODE>
+__device__ __forceinline__ int tile_class(const TcParams& p, const Unit& U, int s, int kt) {
+    if constexpr (MODE == MODE_MASKED) {
+        if (U.nrows[s] <= 0) return 0;
+        const int nkt = (p.T + kTcRows - 1) / kTcRows;
+        return __ldg(p.cls + (long)(U.row0[s] / kTcRows) * nkt + kt);
+    } else {
+        return U.nrows[s] > 0 ? 1 : 0;
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ bool skip_tile(const TcParams& p, const Unit& U, int kt) {
+    if constexpr (MODE == MODE_MASKED)
+        return tile_class<MODE>(p, U, 0, kt) == 0 && tile_class<MODE>(p, U, 1, kt) == 0;
+    else
+        return false;
+}
+
+template <int MODE>
+__device__ __forceinline__ bool unit_active(const TcParams& p, const Unit& U) {
+    if (U.n_kt <= 0) return false;
+    if constexpr (MODE == MODE_MASKED) {
+        for (int kt = 0; kt < U.n_kt; ++kt)
+            if (!skip_tile<MODE>(p, U, kt)) return true;
+        return false;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ kernel --
+template <int D, int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+    using C = TcCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t* qbuf = smem;
+    uint8_t* ring = smem + C::kQBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + C::kRingBytes);
+    uint64_t* empty = full + S;
+    uint64_t* qfull = empty + S;
+    uint64_t* qempty = qfull + 2;
+    uint64_t* sfull = qempty + 2;
+    uint64_t* pfull = sfull + 2;
+    uint64_t* ofull = pfull + 2;
+    uint64_t* drain = ofull + 2;
+    uint64_t* never = drain + 1;  // nothing arrives on it (forced time-out test hook)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qfull[s], 1);
+            mbar_init(&qempty[s], 1);
+            mbar_init(&sfull[s], 1);
+            mbar_init(&pfull[s], kTcRows);
+            mbar_init(&ofull[s], 1);
+        }
+        mbar_init(drain, 1);
+        mbar_init(never, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    int num_units;
+    if constexpr (MODE == MODE_PAGED)
+        num_units = __ldg(p.work_count) * (p.pair_heads ? p.Hkv * (p.g / 2) : p.Hq);
+    else
+        num_units = p.num_units;
+    const int G = gridDim.x;
+    const unsigned long long lim_ns = p.ctx.wait_ns;
+
+    auto fail = [&]() {
+        raise_error(p.ctx, ERR_TIMEOUT_BIT);
+        *abort_flag = 1;
+    };
+
+    if (warp == kProducerWarp) {
+        // ================================================== TMA producer ====
+        int fill = 0, qcnt = 0;
+        bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
+        for (int i = 0; ok; ++i) {
+            if (i * G >= num_units) break;
+            const int u = unit_of(i, G);
+            if (u >= num_units) continue;
+            const Unit U = decode_unit<MODE>(p, u);
+            if (!unit_active<MODE>(p, U)) continue;
+            for (int s = 0; s < 2 && ok; ++s) {
+                if (!mbar_wait_warp(&qempty[s], (qcnt & 1) ^ 1, lim_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&qfull[s], C::kTileBytes);
+#pragma unroll
+                    for (int a = 0; a < C::kAtoms; ++a) {
+                        if constexpr (MODE == MODE_PAGED)
+                            tma_load_4d(qbuf + s * C::kTileBytes + a * C::kAtomBytes, &tm_q, &qfull[s], a * 64,
+                                        U.head[s], U.qtok[s], 0);
+                        else
+                            tma_load_4d(qbuf + s * C::kTileBytes + a * C::kAtomBytes, &tm_q, &qfull[s], a * 64,
+                                        U.head[s], U.qtok[s], U.b);
+                    }
+                }
+            }
+            if (!ok) break;
+            ++qcnt;
+            for (int kt = 0; kt < U.n_kt && ok; ++kt) {
+                if (skip_tile<MODE>(p, U, kt)) continue;
+                for (int which = 0; which < 2; ++which) {  // 0: K tile, 1: V tile
+                    const int stage = fill % S;
+                    if (!mbar_wait_warp(&empty[stage], ((fill / S) & 1) ^ 1, lim_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = ring + stage * C::kTileBytes;
+                    const CUtensorMap* tm = which ? &tm_v : &tm_k;
+                    if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kTileBytes);
+                    __syncwarp();
+                    if constexpr (MODE == MODE_PAGED) {
+                        // lane = a * 8 + blk: one 16-token block of one 64-channel half
+                        if (lane < 8 * C::kAtoms) {
+                            const int a = lane >> 3, blk = lane & 7;
+                            const int lb = kt * 8 + blk;
+                            int phys = p.num_blocks;  // outside the map: zero fill
+                            if (lb * 16 < U.kv_len) {
+                                phys = __ldg(p.bt + (long)U.b * p.mbps + lb);
+                                if (phys < 0 || phys >= p.num_blocks) {
+                                    raise_error(p.ctx, ERR_BOUNDS_BIT);
+                                    phys = p.num_blocks;
+                                }
+                            }
+                            tma_load_4d(dst + a * C::kAtomBytes + blk * 2048, tm, &full[stage], a * 64, 0, U.hk,
+                                        phys);
+                        }
+                    } else {
+                        if (lane == 0) {
+#pragma unroll
+                            for (int a = 0; a < C::kAtoms; ++a)
+                                tma_load_4d(dst + a * C::kAtomBytes, tm, &full[stage], a * 64, U.hk, kt * kTcRows,
+                                            U.b);
+                        }
+                    }
+                    __syncwarp();
+                    ++fill;
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) fail();
+            // let every copy already issued land before the CTA can exit
+            for (int f = max(0, fill - S); f < fill; ++f)
+                (void)mbar_wait_warp(&full[f % S], (f / S) & 1, 1000000000ull, nullptr);
+            if (qcnt > 0)
+                for (int s = 0; s < 2; ++s)
+                    (void)mbar_wait_warp(&qfull[s], (qcnt - 1) & 1, 1000000000ull, nullptr);
+        }
+    } else if (warp == kMmaWarp) {
+        // ===================================================== MMA issuer ===
+        constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+        const uint32_t q_addr = smem_u32(qbuf), ring_addr = smem_u32(ring);
+        const uint32_t s_col[2] = {C::kS0, C::kS1}, o_col[2] = {C::kO0, C::kO1};
+        int cons = 0, ucnt = 0, pc[2] = {0, 0};
+        bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
+
+        auto wait_v = [&](int vidx, int vkt, const Unit& U) -> bool {
+            if (!mbar_wait_warp(&full[vidx % S], (vidx / S) & 1, lim_ns, abort_flag)) return false;
+            if constexpr (MODE == MODE_PAGED) {
+                // Rows past the context inside the last partly filled block
+                // may hold stale words; zero them so a zero probability never
+                // meets a non-finite value.
+                const int kv0 = vkt * kTcRows;
+                const int z0 = U.kv_len - kv0;
+                const int z1 = min(kTcRows, ((U.kv_len + 15) & ~15) - kv0);
+                if (z0 < z1) {
+                    uint8_t* base = ring + (vidx % S) * C::kTileBytes;
+                    const int n16 = (z1 - z0) * C::kAtoms * 8;
+                    for (int e = lane; e < n16; e += 32) {
+                        const int row = z0 + e / (C::kAtoms * 8);
+                        const int a = (e / 8) % C::kAtoms;
+                        *reinterpret_cast<uint4*>(base + a * C::kAtomBytes + row * 128 + (e % 8) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+            }
+            return true;
+        };
+        auto issue_qk = [&](int s, int kidx) {
+            const uint32_t kb = ring_addr + (kidx % S) * C::kTileBytes;
+            const uint32_t qb = q_addr + s * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
+                umma_ss(tbase + s_col[s], smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                        kIdescQK, kk > 0);
+            }
+        };
+        auto issue_pv = [&](int s, int vidx, bool acc_first) {
+            const uint32_t vb = ring_addr + (vidx % S) * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kTcRows / 16; ++kk)
+                umma_ts(tbase + o_col[s], tbase + s_col[s] + kk * 8,
+                        smem_desc_sw128(vb + kk * 2048, C::kAtomBytes, 1024), kIdescPV, (acc_first || kk > 0));
+        };
+
+        for (int i = 0; ok; ++i) {
+            if (i * G >= num_units) break;
+            const int u = unit_of(i, G);
+            if (u >= num_units) continue;
+            const Unit U = decode_unit<MODE>(p, u);
+            if (!unit_active<MODE>(p, U)) continue;
+            for (int s = 0; s < 2; ++s)
+                if (!mbar_wait_warp(&qfull[s], ucnt & 1, lim_ns, abort_flag)) ok = false;
+            if (!ok) break;
+            ++ucnt;
+            int it = 0, prev_v = -1, prev_kt = -1;
+            for (int kt = 0; kt < U.n_kt && ok; ++kt) {
+                if (skip_tile<MODE>(p, U, kt)) continue;
+                const int kidx = cons + 2 * it;
+                if (!mbar_wait_warp(&full[kidx % S], (kidx / S) & 1, lim_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int s = 0; s < 2 && ok; ++s) {
+                    if (it > 0) {
+                        if (s == 0 && !wait_v(prev_v, prev_kt, U)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait_warp(&pfull[s], pc[s] & 1, lim_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        ++pc[s];
+                        tc_fence_after();
+                        if (lane == 0) issue_pv(s, prev_v, it > 1);
+                    }
+                    if (lane == 0) {
+                        issue_qk(s, kidx);
+                        umma_commit(&sfull[s]);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    umma_commit(&empty[kidx % S]);
+                    if (it > 0) umma_commit(&empty[prev_v % S]);
+                }
+                __syncwarp();
+                prev_v = kidx + 1;
+                prev_kt = kt;
+                ++it;
+            }
+            if (!ok) break;
+            if (lane == 0) {
+                umma_commit(&qempty[0]);
+                umma_commit(&qempty[1]);
+            }
+            if (!wait_v(prev_v, prev_kt, U)) {
+                ok = false;
+                break;
+            }
+            for (int s = 0; s < 2 && ok; ++s) {
+                if (!mbar_wait_warp(&pfull[s], pc[s] & 1, lim_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++pc[s];
+                tc_fence_after();
+                if (lane == 0) {
+                    issue_pv(s, prev_v, it > 1);
+                    umma_commit(&ofull[s]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(&empty[prev_v % S]);
+            __syncwarp();
+            cons += 2 * it;
+        }
+        if (!ok && lane == 0) fail();
+        // every MMA issued above completes before TMEM is released
+        if (lane == 0) umma_commit(drain);
+        __syncwarp();
+        (void)mbar_wait_bounded(drain, 0, 1000000000ull, nullptr);
+    } else {
+        // ======================================================== softmax ===
+        const int s = warp >> 2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t trow = tbase + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t s_col = s ? C::kS1 : C::kS0;
+        const uint32_t o_col = s ? C::kO1 : C::kO0;
+        int sc = 0, oc = 0;
+        bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
+        for (int i = 0; ok; ++i) {
+            if (i * G >= num_units) break;
+            const int u = unit_of(i, G);
+            if (u >= num_units) continue;
+            const Unit U = decode_unit<MODE>(p, u);
+            const bool valid = r < U.nrows[s];
+            const int row = U.row0[s] + r;  // row within T (dense) or within the chunk (paged)
+            uint16_t* orow;
+            if constexpr (MODE == MODE_PAGED)
+                orow = p.out + ((long)U.qtok[s] + r) * p.Hq * D + (long)U.head[s] * D;
+            else
+                orow = p.out + (((long)U.b * p.T + row) * p.Hq + U.head[s]) * D;
+            float* lse_ptr = nullptr;
+            if constexpr (MODE != MODE_PAGED)
+                if (p.lse && valid) lse_ptr = p.lse + ((long)U.b * p.Hq + U.head[s]) * p.T + row;
+            if (!unit_active<MODE>(p, U)) {
+                if (valid) {
+                    for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+                    if (lse_ptr) *lse_ptr = -INFINITY;
+                }
+                continue;
+            }
+            // key j is visible when j <= row + pos_off (causal) and j < kv_len
+            const int vis_end = p.causal ? min(U.kv_len, row + U.pos_off + 1) : U.kv_len;
+            float m = -INFINITY, l = 0.f;
+            int it = 0;
+            for (int kt = 0; kt < U.n_kt; ++kt) {
+                if (skip_tile<MODE>(p, U, kt)) continue;
+                if (!mbar_wait_warp(&sfull[s], sc & 1, lim_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++sc;
+                tc_fence_after();
+                const int kv0 = kt * kTcRows;
+                const int lim = vis_end - kv0;  // visible columns of this tile: [0, lim)
+                const int cls = tile_class<MODE>(p, U, s, kt);
+                const float* mrow = (cls == 2 && valid) ? p.mask + (long)row * p.T + kv0 : nullptr;
+                // scaled, masked score of column j (base-2 logits)
+                auto logit = [&](float sv, int j) -> float {
+                    if (cls == 0 || j >= lim) return -INFINITY;
+                    if (mrow) return fmaf(sv, p.scale_log2, __ldg(mrow + j) * kLog2e);
+                    return sv * p.scale_log2;
+                };
+                // pass 1: row max, 32 columns at a time
+                float mx = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(trow + s_col + c * 32, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, logit(__uint_as_float(raw[j]), c * 32 + j));
+                }
+                const float m_new = fmaxf(m, mx);
+                const bool need = m_new > m + kRescaleThreshold;
+                float alpha = 1.f;
+                const bool warp_rescale = __any_sync(0xffffffffu, need);
+                if (warp_rescale) {
+                    alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - m_new);
+                    l *= alpha;
+                    m = m_new;
+                }
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                // pass 2: P = 2^(logit - m) as bf16 into the first 64 columns of S.
+                // Chunk c reads S columns [32c, 32c+32) and writes P columns
+                // [16c, 16c+16), which only overlap S columns already read.
+                float rs = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(trow + s_col + c * 32, raw);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = fast_exp2(logit(__uint_as_float(raw[2 * j]), c * 32 + 2 * j) - m_use);
+                        const float p1 = fast_exp2(logit(__uint_as_float(raw[2 * j + 1]), c * 32 + 2 * j + 1) - m_use);
+                        rs += p0 + p1;
+                        pk[j] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(trow + s_col + c * 16, pk);
+                }
+                l += rs;
+                if (warp_rescale && it > 0) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t raw[32];
+                        tmem_ld32(trow + o_col + c * 32, raw);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(__uint_as_float(raw[j]) * alpha);
+                        tmem_st32(trow + o_col + c * 32, raw);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&pfull[s]);
+                ++it;
+            }
+            if (!ok) break;
+            if (!mbar_wait_warp(&ofull[s], oc & 1, lim_ns, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ++oc;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(trow + o_col + c * 32, raw);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[j] = pack_bf16x2(__uint_as_float(raw[2 * j]) * inv_l, __uint_as_float(raw[2 * j + 1]) * inv_l);
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+                    dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+                }
+            }
+            if (lse_ptr) *lse_ptr = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
+        if (!ok && lane == 0) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
+}
+
+// ----------------------------------------------------------- mask order ---
+// Orders query tiles by decreasing number of KV tiles that are not entirely
+// masked (longest first), from the tile classes of the additive mask.
+__global__ void __launch_bounds__(256) mask_order_kernel(const uint8_t* __restrict__ cls, int nqt, int nkt,
+                                                         int causal, int32_t* __restrict__ order) {
+    extern __shared__ int cost[];
+    for (int q = threadIdx.x; q < nqt; q += blockDim.x) {
+        int c = 0;
+        const int kend = causal ? min(nkt, q + 1) : nkt;
+        for (int k = 0; k < kend; ++k) c += cls[(long)q * nkt + k] != 0;
+        cost[q] = c;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < nqt; q += blockDim.x) {
+        int rank = 0;
+        const int cq = cost[q];
+        for (int o = 0; o < nqt; ++o) rank += (cost[o] > cq) || (cost[o] == cq && o < q);
+        order[rank] = q;
+    }
+}
+
+fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, cudaStream_t s);
+
+// ------------------------------------------------------------ launchers ---
+template <int D, int MODE>
+static fa_status launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p,
+                           int grid, cudaStream_t s) {
+    static bool attr_done = false;  // setting the attribute twice is harmless
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(attn_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcCfg<D>::kSmem) != cudaSuccess)
+            return FA_ERR_CUDA;
+        attr_done = true;
+    }
+    attn_tc_kernel<D, MODE><<<grid, kTcThreads, TcCfg<D>::kSmem, s>>>(tq, tk, tv, p);
+    return cuda_status(cudaGetLastError());
+}
+
+template <int MODE>
+static fa_status launch_tc_d(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const TcParams& p, int grid, cudaStream_t s) {
+    return d == 128 ? launch_tc<128, MODE>(tq, tk, tv, p, grid, s) : launch_tc<64, MODE>(tq, tk, tv, p, grid, s);
+}
+
+static fa_status dense_maps(const void* q, const void* k, const void* v, int B, int T, int Hq, int Hkv, int d,
+                            CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
+    const uint32_t box[4] = {64, 1, (uint32_t)kTcRows, 1};
+    const uint64_t dq[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)T, (uint64_t)B};
+    const uint64_t sq[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)T * Hq * d * 2};
+    const uint64_t dk[4] = {(uint64_t)d, (uint64_t)Hkv, (uint64_t)T, (uint64_t)B};
+    const uint64_t sk[3] = {(uint64_t)d * 2, (uint64_t)Hkv * d * 2, (uint64_t)T * Hkv * d * 2};
+    fa_status st = encode_tmap_bf16_4d(tq, q, dq, sq, box);
+    if (st == FA_OK) st = encode_tmap_bf16_4d(tk, k, dk, sk, box);
+    if (st == FA_OK) st = encode_tmap_bf16_4d(tv, v, dk, sk, box);
+    return st;
+}
+
+static fa_status check_prefill_args(const void* q, const void* k, const void* v, const void* out, int B, int T,
+                                    int Hq, int Hkv, int d) {
+    if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0) return FA_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || Hq % Hkv != 0) return FA_ERR_UNSUPPORTED;
+    if (B == 0 || T == 0) return FA_OK;
+    if (!q || !k || !v || !out) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+static TcParams base_params(int B, int T, int Hq, int Hkv, int causal, float scale, void* out, float* lse,
+                            const DevCtx& ctx) {
+    TcParams p{};
+    p.B = B;
+    p.T = T;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = Hq / Hkv;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    p.pair_heads = (p.g % 2 == 0) ? 1 : 0;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.ctx = ctx;
+    return p;
+}
+
+static int dense_units(const TcParams& p) {
+    const int nqt = (p.T + kTcRows - 1) / kTcRows;
+    return p.pair_heads ? p.B * p.Hkv * (p.g / 2) * nqt : p.B * p.Hq * ((nqt + 1) / 2);
+}
+
+fa_status launch_paged_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                               const int32_t* ctx_lens, const int32_t* q_lens, const int32_t* q_start,
+                               const int32_t* work_list, const int32_t* work_count, void* out, int num_seqs,
+                               int mbps, int num_blocks, int Hq, int Hkv, int d, int causal, float scale,
+                               int total_q, cudaStream_t s, const DevCtx& ctx) {
+    (void)num_seqs;
+    CUtensorMap tq, tk, tv;
+    const uint32_t qbox[4] = {64, 1, (uint32_t)kTcRows, 1};
+    const uint64_t dq[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
+    const uint64_t sq[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
+    const uint32_t cbox[4] = {64, 16, 1, 1};
+    const uint64_t dc[4] = {(uint64_t)d, 16, (uint64_t)Hkv, (uint64_t)num_blocks};
+    const uint64_t scs[3] = {(uint64_t)d * 2, (uint64_t)16 * d * 2, (uint64_t)Hkv * 16 * d * 2};
+    fa_status st = encode_tmap_bf16_4d(&tq, q, dq, sq, qbox);
+    if (st == FA_OK) st = encode_tmap_bf16_4d(&tk, k_cache, dc, scs, cbox);
+    if (st == FA_OK) st = encode_tmap_bf16_4d(&tv, v_cache, dc, scs, cbox);
+    if (st != FA_OK) return st;
+    TcParams p = base_params(0, 0, Hq, Hkv, causal, scale, out, nullptr, ctx);
+    p.bt = block_table;
+    p.ctx_lens = ctx_lens;
+    p.q_lens = q_lens;
+    p.q_start = q_start;
+    p.work_list = work_list;
+    p.work_count = work_count;
+    p.mbps = mbps;
+    p.num_blocks = num_blocks;
+    return launch_tc_d<MODE_PAGED>(d, tq, tk, tv, p, sm_count(), s);
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv, int d,
+                     int causal, float scale, float* lse, fa_stream_t stream) {
+    set_launch_count(0);
+    fa_status st = check_prefill_args(q, k, v, out, B, T, Hq, Hkv, d);
+    if (st != FA_OK || B == 0 || T == 0) return st;
+    if ((st = check_device()) != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    CUtensorMap tq, tk, tv;
+    if ((st = dense_maps(q, k, v, B, T, Hq, Hkv, d, &tq, &tk, &tv)) != FA_OK) return st;
+    TcParams p = base_params(B, T, Hq, Hkv, causal, scale, out, lse, ctx);
+    p.num_units = dense_units(p);
+    const int grid = std::min(p.num_units, sm_count());
+    st = launch_tc_d<MODE_DENSE>(d, tq, tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
+size_t fa_prefill_masked_workspace_size(int T) {
+    if (T <= 0) return 0;
+    const size_t nt = (size_t)(T + kTcRows - 1) / kTcRows;
+    return align256(nt * nt) + align256(sizeof(int32_t) * nt);
+}
+
+fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const float* mask, void* out, int B, int T,
+                            int Hq, int Hkv, int d, int causal, float scale, float* lse, void* ws, size_t ws_bytes,
+                            fa_stream_t stream) {
+    set_launch_count(0);
+    fa_status st = check_prefill_args(q, k, v, out, B, T, Hq, Hkv, d);
+    if (st != FA_OK || B == 0 || T == 0) return st;
+    if (!mask) return fa_prefill(q, k, v, out, B, T, Hq, Hkv, d, causal, scale, lse, stream);
+    if (!ws || ws_bytes < fa_prefill_masked_workspace_size(T) || (reinterpret_cast<uintptr_t>(ws) & 255))
+        return FA_ERR_WORKSPACE;
+    if ((st = check_device()) != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    CUtensorMap tq, tk, tv;
+    if ((st = dense_maps(q, k, v, B, T, Hq, Hkv, d, &tq, &tk, &tv)) != FA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int nt = (T + kTcRows - 1) / kTcRows;
+    uint8_t* cls = static_cast<uint8_t*>(ws);
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + align256((size_t)nt * nt));
+    if ((st = launch_mask_classify(mask, T, T, cls, s)) != FA_OK) return st;
+    if ((size_t)nt * sizeof(int) > 200 * 1024) return FA_ERR_UNSUPPORTED;
+    if (nt * sizeof(int) > 48 * 1024 &&
+        cudaFuncSetAttribute(mask_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, nt * (int)sizeof(int)) !=
+            cudaSuccess)
+        return FA_ERR_CUDA;
+    mask_order_kernel<<<1, 256, nt * sizeof(int), s>>>(cls, nt, nt, causal ? 1 : 0, order);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    TcParams p = base_params(B, T, Hq, Hkv, causal, scale, out, lse, ctx);
+    p.mask = mask;
+    p.cls = cls;
+    p.qt_order = order;
+    p.num_units = dense_units(p);
+    const int grid = std::min(p.num_units, sm_count());
+    st = launch_tc_d<MODE_MASKED>(d, tq, tk, tv, p, grid, s);
+    if (st == FA_OK) set_launch_count(3);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,223 @@
+// Memory-bound helper kernels of libfattn:
+//   * fused KV-cache append ("Fast Attention Kernels and Operator Fusion",
+//     section "Operator Fusion", fusion list: updating the KV cache while
+//     transforming key and value tensors);
+//   * fp32 -> bf16 staging cast;
+//   * block-table gather test hook ("Paged Attention Kernels": translate each
+//     logical position through the block table);
+//   * additive-mask tile classifier used by the masked prefill
+//     ("FlashAttention-Style Kernels", attention equation with additive M).
+// All of them move data with 16-byte vector accesses and are sized by
+// grid-stride loops over a multiple of the SM count.
+#include "host_common.cuh"
+
+namespace fa {
+
+constexpr int kBlock = 16;  // tokens per cache block
+
+// ------------------------------------------------------------ append ------
+// One thread moves one 16-byte chunk (8 bf16) of one (token, head) row of K
+// and the same chunk of V.  Input rows are contiguous [N, Hkv, d]; the cache
+// row of (slot, head) starts at ((slot/16 * Hkv + head) * 16 + slot%16) * d.
+template <bool kF32>
+__global__ void __launch_bounds__(256) cache_append_kernel(const void* __restrict__ k, const void* __restrict__ v,
+                                                           uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
+                                                           const int32_t* __restrict__ slots, int N, int Hkv,
+                                                           int d, int num_blocks, DevCtx ctx) {
+    const int cpr = d >> 3;  // chunks per row
+    const long total = (long)N * Hkv * cpr;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int c = (int)(idx % cpr);
+        const long row = idx / cpr;  // token * Hkv + head
+        const int h = (int)(row % Hkv);
+        const long tok = row / Hkv;
+        const int slot = __ldg(slots + tok);
+        if (slot < 0) continue;
+        if (slot >= num_blocks * kBlock) {
+            raise_error(ctx, ERR_BOUNDS_BIT);
+            continue;
+        }
+        const long dst = (((long)(slot / kBlock) * Hkv + h) * kBlock + (slot % kBlock)) * d + c * 8;
+        uint4 kv4, vv4;
+        if constexpr (kF32) {
+            const float4* ks = reinterpret_cast<const float4*>(static_cast<const float*>(k) + row * d + c * 8);
+            const float4* vs = reinterpret_cast<const float4*>(static_cast<const float*>(v) + row * d + c * 8);
+            float4 a = __ldg(ks), b = __ldg(ks + 1), e = __ldg(vs), f = __ldg(vs + 1);
+            kv4 = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                             pack_bf16x2(b.z, b.w));
+            vv4 = make_uint4(pack_bf16x2(e.x, e.y), pack_bf16x2(e.z, e.w), pack_bf16x2(f.x, f.y),
+                             pack_bf16x2(f.z, f.w));
+        } else {
+            kv4 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(k) + row * d + c * 8));
+            vv4 = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(v) + row * d + c * 8));
+        }
+        *reinterpret_cast<uint4*>(kc + dst) = kv4;
+        *reinterpret_cast<uint4*>(vc + dst) = vv4;
+    }
+}
+
+// ------------------------------------------------------------- stage ------
+__global__ void __launch_bounds__(256) stage_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
+                                                         size_t n) {
+    const size_t n8 = n / 8;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const float4* s = reinterpret_cast<const float4*>(src) + 2 * i;
+        float4 a = __ldg(s), b = __ldg(s + 1);
+        *reinterpret_cast<uint4*>(dst + 8 * i) =
+            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+    }
+    if (blockIdx.x == 0)
+        for (size_t i = n8 * 8 + threadIdx.x; i < n; i += blockDim.x) {
+            __nv_bfloat16 b = __float2bfloat16_rn(src[i]);
+            dst[i] = *reinterpret_cast<uint16_t*>(&b);
+        }
+}
+
+// ------------------------------------------------------------ gather ------
+__global__ void __launch_bounds__(256) gather_kv_kernel(const uint16_t* __restrict__ cache,
+                                                        const int32_t* __restrict__ bt,
+                                                        const int32_t* __restrict__ ctx_lens,
+                                                        uint16_t* __restrict__ out, int num_seqs, int mbps,
+                                                        int num_blocks, int Hkv, int d, int max_ctx, DevCtx ctx) {
+    const int cpr = d >> 3;
+    const long per_seq = (long)max_ctx * Hkv * cpr;
+    const long total = per_seq * num_seqs;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int s = (int)(idx / per_seq);
+        const long r = idx % per_seq;
+        const int c = (int)(r % cpr);
+        const int h = (int)((r / cpr) % Hkv);
+        const int t = (int)(r / ((long)cpr * Hkv));
+        const int L = __ldg(ctx_lens + s);
+        if (t >= L) continue;
+        if (L > mbps * kBlock) {
+            raise_error(ctx, ERR_BOUNDS_BIT);
+            continue;
+        }
+        const int phys = __ldg(bt + (long)s * mbps + t / kBlock);
+        if (phys < 0 || phys >= num_blocks) {
+            raise_error(ctx, ERR_BOUNDS_BIT);
+            continue;
+        }
+        const long src = (((long)phys * Hkv + h) * kBlock + t % kBlock) * d + c * 8;
+        const long dst = (((long)s * max_ctx + t) * Hkv + h) * d + c * 8;
+        *reinterpret_cast<uint4*>(out + dst) = __ldg(reinterpret_cast<const uint4*>(cache + src));
+    }
+}
+
+// ------------------------------------------------------- mask classes -----
+// One CTA per 128x128 tile of the mask: class 0 when every in-range element
+// is -inf, 1 when every element is exactly 0, 2 otherwise.  Rows are read
+// with coalesced 16-byte loads when the row length allows it.
+__global__ void __launch_bounds__(256) mask_classify_kernel(const float* __restrict__ M, int Tq, int Tk,
+                                                            uint8_t* __restrict__ cls) {
+    const int tj = blockIdx.x, ti = blockIdx.y;
+    const int i0 = ti * 128, j0 = tj * 128;
+    const int rows = min(128, Tq - i0), cols = min(128, Tk - j0);
+    bool all_ninf = true, all_zero = true;
+    const bool vec = (Tk % 4 == 0) && (cols == 128);
+    if (vec) {
+        // 32 threads cover one 512-byte row; 8 rows per pass
+        const int lane = threadIdx.x & 31, rgrp = threadIdx.x >> 5;
+        for (int r = rgrp; r < rows; r += 8) {
+            float4 x = __ldg(reinterpret_cast<const float4*>(M + (long)(i0 + r) * Tk + j0) + lane);
+            all_ninf &= (x.x == -INFINITY) & (x.y == -INFINITY) & (x.z == -INFINITY) & (x.w == -INFINITY);
+            all_zero &= (x.x == 0.f) & (x.y == 0.f) & (x.z == 0.f) & (x.w == 0.f);
+        }
+    } else {
+        for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
+            const float x = __ldg(M + (long)(i0 + e / cols) * Tk + j0 + e % cols);
+            all_ninf &= (x == -INFINITY);
+            all_zero &= (x == 0.f);
+        }
+    }
+    const int n_inf = __syncthreads_and(all_ninf);
+    const int n_zero = __syncthreads_and(all_zero);
+    if (threadIdx.x == 0) cls[(long)ti * gridDim.x + tj] = (uint8_t)(n_inf ? 0 : (n_zero ? 1 : 2));
+}
+
+// Launched from the masked prefill entry point.
+fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, cudaStream_t s) {
+    dim3 grid((Tk + 127) / 128, (Tq + 127) / 128);
+    mask_classify_kernel<<<grid, 256, 0, s>>>(M, Tq, Tk, cls);
+    return cuda_status(cudaGetLastError());
+}
+
+static int grid_for(long work, int per_cta) {
+    long g = (work + per_cta - 1) / per_cta;
+    long cap = (long)sm_count() * 8;
+    if (g > cap) g = cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_cache_append(const void* k, const void* v, void* k_cache, void* v_cache, const int32_t* slot_mapping,
+                          int N, int Hkv, int d, int num_blocks, fa_dtype in_dtype, fa_stream_t stream) {
+    set_launch_count(0);
+    if (N < 0 || Hkv <= 0 || num_blocks < 0) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (in_dtype != FA_BF16 && in_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+    if (N == 0) return FA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return FA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return FA_ERR_INVALID_ARG;
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    const long work = (long)N * Hkv * (d / 8);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FA_F32)
+        cache_append_kernel<true><<<grid_for(work, 256), 256, 0, s>>>(k, v, static_cast<uint16_t*>(k_cache),
+                                                                      static_cast<uint16_t*>(v_cache), slot_mapping,
+                                                                      N, Hkv, d, num_blocks, ctx);
+    else
+        cache_append_kernel<false><<<grid_for(work, 256), 256, 0, s>>>(k, v, static_cast<uint16_t*>(k_cache),
+                                                                       static_cast<uint16_t*>(v_cache),
+                                                                       slot_mapping, N, Hkv, d, num_blocks, ctx);
+    st = cuda_status(cudaGetLastError());
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
+fa_status fa_stage_bf16(const float* src, void* dst, size_t n, fa_stream_t stream) {
+    set_launch_count(0);
+    if (n == 0) return FA_OK;
+    if (!src || !dst || !aligned16(src) || !aligned16(dst)) return FA_ERR_INVALID_ARG;
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    stage_bf16_kernel<<<grid_for((long)(n / 8 + 1), 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        src, static_cast<uint16_t*>(dst), n);
+    st = cuda_status(cudaGetLastError());
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
+fa_status fa_debug_gather_kv(const void* cache, const int32_t* block_table, const int32_t* ctx_lens, void* out,
+                             int num_seqs, int max_blocks_per_seq, int num_blocks, int Hkv, int d, int max_ctx,
+                             fa_stream_t stream) {
+    set_launch_count(0);
+    if (num_seqs < 0 || max_blocks_per_seq < 0 || num_blocks < 0 || Hkv <= 0 || max_ctx < 0)
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || max_ctx == 0) return FA_OK;
+    if (!cache || !block_table || !ctx_lens || !out || !aligned16(cache) || !aligned16(out))
+        return FA_ERR_INVALID_ARG;
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    const long work = (long)num_seqs * max_ctx * Hkv * (d / 8);
+    gather_kv_kernel<<<grid_for(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(cache), block_table, ctx_lens, static_cast<uint16_t*>(out), num_seqs,
+        max_blocks_per_seq, num_blocks, Hkv, d, max_ctx, ctx);
+    st = cuda_status(cudaGetLastError());
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,235 @@
+"""ctypes binding of libfattn (include/fattn.h).
+
+Argument marshalling only: every function here checks dtypes/shapes, passes
+device pointers, sizes and the current CUDA stream to the C entry point of the
+same name, and raises ``FattnError`` on a non-OK status.  All arithmetic runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
+importing this module fails loudly when ``libfattn.so`` has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfattn.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BOUNDS, FA_ERR_WORKSPACE = range(7)
+FA_BF16, FA_F32 = 0, 1
+
+# every symbol declared in include/fattn.h
+EXPORTS = [
+    "fa_status_string", "fa_prefill", "fa_prefill_masked_workspace_size", "fa_prefill_masked", "fa_stage_bf16",
+    "fa_cache_append", "fa_paged_attn_workspace_size", "fa_paged_attn", "fa_get_error", "fa_debug_gather_kv",
+    "fa_debug_set_wait_limit", "fa_debug_force_timeout", "fa_last_launch_count",
+]
+
+
+class FattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with paged_kv_cache_tiled_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    Z = ctypes.c_size_t
+    sig = {
+        "fa_status_string": (ctypes.c_char_p, [I]),
+        "fa_prefill": (I, [P, P, P, P, I, I, I, I, I, I, F, P, P]),
+        "fa_prefill_masked_workspace_size": (Z, [I]),
+        "fa_prefill_masked": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, Z, P]),
+        "fa_stage_bf16": (I, [P, P, Z, P]),
+        "fa_cache_append": (I, [P, P, P, P, P, I, I, I, I, I, P]),
+        "fa_paged_attn_workspace_size": (Z, [I, I, I, I, I, I]),
+        "fa_paged_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, Z, P]),
+        "fa_get_error": (I, [P]),
+        "fa_debug_gather_kv": (I, [P, P, P, P, I, I, I, I, I, I, P]),
+        "fa_debug_set_wait_limit": (None, [ctypes.c_ulonglong]),
+        "fa_debug_force_timeout": (None, [I]),
+        "fa_last_launch_count": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.fa_status_string(int(status)).decode()
+
+
+fa_status_string = status_string
+
+
+def _check(st: int, where: str):
+    if st != FA_OK:
+        raise FattnError(st, where)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+# ------------------------------------------------------------------ prefill
+def fa_prefill(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None, stream=None):
+    """softmax(scale * Q K^T [+ causal mask]) V for q [B,T,Hq,d], k/v [B,T,Hkv,d] (bf16)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, 4)
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    _check(_lib.fa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, d, int(causal), float(scale),
+                           _ptr(lse), _stream(stream)), "fa_prefill")
+    return out
+
+
+def fa_prefill_masked_workspace_size(T: int) -> int:
+    return int(_lib.fa_prefill_masked_workspace_size(int(T)))
+
+
+def fa_prefill_masked(q, k, v, mask, causal: bool = False, scale: float | None = None, out=None, lse=None, ws=None,
+                      stream=None):
+    """softmax(scale * Q K^T + M [+ causal]) V with an additive fp32 mask M [T, T]."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, 4)
+    _need(mask, "mask", torch.float32, 2)
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = fa_prefill_masked_workspace_size(T)
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(_lib.fa_prefill_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), B, T, Hq, Hkv, d, int(causal),
+                                  float(scale), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "fa_prefill_masked")
+    return out
+
+
+def fa_stage_bf16(src, dst=None, stream=None):
+    """fp32 -> bf16 (round to nearest even)."""
+    _need(src, "src", torch.float32)
+    if dst is None:
+        dst = torch.empty(src.shape, dtype=torch.bfloat16, device=src.device)
+    _need(dst, "dst", torch.bfloat16)
+    _check(_lib.fa_stage_bf16(_ptr(src), _ptr(dst), src.numel(), _stream(stream)), "fa_stage_bf16")
+    return dst
+
+
+# -------------------------------------------------------------------- paged
+def fa_cache_append(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """Writes k/v [N, Hkv, d] (bf16 or fp32) into the caches [num_blocks, Hkv, 16, d] at slot_mapping[N]."""
+    if k.dtype not in (torch.bfloat16, torch.float32) or v.dtype != k.dtype:
+        raise ValueError("k, v must both be bf16 or both fp32")
+    _need(k, "k", k.dtype, 3)
+    _need(v, "v", k.dtype, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    N, Hkv, d = k.shape
+    dt = FA_F32 if k.dtype == torch.float32 else FA_BF16
+    _check(_lib.fa_cache_append(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hkv, d,
+                                k_cache.shape[0], dt, _stream(stream)), "fa_cache_append")
+
+
+def fa_paged_attn_workspace_size(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q) -> int:
+    return int(_lib.fa_paged_attn_workspace_size(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q))
+
+
+def fa_paged_attn(q, k_cache, v_cache, block_table, ctx_lens, q_lens, causal: bool = True,
+                  scale: float | None = None, out=None, max_q_len: int | None = None, ws=None, stream=None):
+    """Attention of packed queries q [total_q, Hq, d] against the paged cache."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    _need(q_lens, "q_lens", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    num_seqs, mbps = block_table.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if max_q_len is None:
+        max_q_len = total_q
+    nbytes = fa_paged_attn_workspace_size(num_seqs, mbps, Hq, Hkv, d, total_q)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(_lib.fa_paged_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens),
+                              _ptr(q_lens), _ptr(out), num_seqs, mbps, num_blocks, Hq, Hkv, d, bs, int(causal),
+                              float(scale), total_q, int(max_q_len), _ptr(ws), ws.numel() * ws.element_size(),
+                              _stream(stream)), "fa_paged_attn")
+    return out
+
+
+# --------------------------------------------------------------- utilities
+def fa_get_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return int(_lib.fa_get_error(_stream(stream)))
+
+
+def fa_debug_gather_kv(cache, block_table, ctx_lens, max_ctx: int, out=None, stream=None):
+    _need(cache, "cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    num_blocks, Hkv, _, d = cache.shape
+    num_seqs, mbps = block_table.shape
+    if out is None:
+        out = torch.zeros(num_seqs, max_ctx, Hkv, d, dtype=torch.bfloat16, device=cache.device)
+    _check(_lib.fa_debug_gather_kv(_ptr(cache), _ptr(block_table), _ptr(ctx_lens), _ptr(out), num_seqs, mbps,
+                                   num_blocks, Hkv, d, max_ctx, _stream(stream)), "fa_debug_gather_kv")
+    return out
+
+
+def fa_debug_set_wait_limit(nanoseconds: int):
+    _lib.fa_debug_set_wait_limit(int(nanoseconds))
+
+
+def fa_debug_force_timeout(enable: bool):
+    _lib.fa_debug_force_timeout(int(bool(enable)))
+
+
+def fa_last_launch_count() -> int:
+    return int(_lib.fa_last_launch_count())

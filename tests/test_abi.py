@@ -1,0 +1,80 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, and rejects malformed or unsupported arguments on the host before
+any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fattn():
+    from paged_kv_cache_tiled_gb300 import build
+    build.build()
+    from paged_kv_cache_tiled_gb300 import fattn as F
+    return F
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "fattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_header_symbol(fattn):
+    syms = header_symbols()
+    assert len(syms) >= 12
+    lib = ctypes.CDLL(fattn.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert sorted(fattn.EXPORTS) == syms
+
+
+def test_status_strings(fattn):
+    assert fattn.status_string(0) == "FA_OK"
+    assert fattn.status_string(fattn.FA_ERR_BOUNDS) == "FA_ERR_BOUNDS"
+    assert fattn.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_host_validation(fattn):
+    lib = fattn.library()
+    P = ctypes.c_void_p
+    dummy = P(4096)  # never dereferenced: validation fails first
+    # negative sizes
+    assert lib.fa_prefill(dummy, dummy, dummy, dummy, -1, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_INVALID_ARG
+    # unsupported head dim / GQA ratio
+    assert lib.fa_prefill(dummy, dummy, dummy, dummy, 1, 16, 4, 2, 96, 1, 0.1, None, None) == fattn.FA_ERR_UNSUPPORTED
+    assert lib.fa_prefill(dummy, dummy, dummy, dummy, 1, 16, 5, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_UNSUPPORTED
+    # empty problems are no-ops
+    assert lib.fa_prefill(None, None, None, None, 0, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_OK
+    # null pointers / misalignment
+    assert lib.fa_prefill(None, dummy, dummy, dummy, 1, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_prefill(P(4097), dummy, dummy, dummy, 1, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_INVALID_ARG
+    # paged: block size other than 16 is unsupported
+    assert lib.fa_paged_attn(dummy, dummy, dummy, dummy, dummy, dummy, dummy, 2, 4, 8, 4, 2, 64, 32, 1, 0.1, 2, 1,
+                             dummy, 1 << 20, None) == fattn.FA_ERR_UNSUPPORTED
+    # paged: missing / short workspace
+    need = lib.fa_paged_attn_workspace_size(2, 4, 4, 2, 64, 2)
+    assert need > 0
+    assert lib.fa_paged_attn(dummy, dummy, dummy, dummy, dummy, dummy, dummy, 2, 4, 8, 4, 2, 64, 16, 1, 0.1, 2, 1,
+                             dummy, need - 1, None) == fattn.FA_ERR_WORKSPACE
+    assert lib.fa_paged_attn(dummy, dummy, dummy, dummy, dummy, dummy, dummy, 2, 4, 8, 4, 2, 64, 16, 1, 0.1, 2, 1,
+                             None, need, None) == fattn.FA_ERR_WORKSPACE
+    # append: bad dtype code, head dim
+    assert lib.fa_cache_append(dummy, dummy, dummy, dummy, dummy, 4, 2, 64, 8, 7, None) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_cache_append(dummy, dummy, dummy, dummy, dummy, 4, 2, 80, 8, 0, None) == fattn.FA_ERR_UNSUPPORTED
+    assert lib.fa_cache_append(None, None, None, None, None, 0, 2, 64, 8, 0, None) == fattn.FA_OK
+    # masked prefill workspace
+    assert lib.fa_prefill_masked_workspace_size(16384) >= 128 * 128 + 128 * 4
+    assert lib.fa_prefill_masked(dummy, dummy, dummy, dummy, dummy, 1, 300, 4, 2, 64, 0, 0.1, None, dummy, 10,
+                                 None) == fattn.FA_ERR_WORKSPACE
+
+
+def test_workspace_sizes_grow(fattn):
+    a = fattn.fa_paged_attn_workspace_size(64, 256, 12, 2, 128, 64)
+    b = fattn.fa_paged_attn_workspace_size(128, 256, 12, 2, 128, 128)
+    assert 0 < a < b
+    assert a % 256 == 0
