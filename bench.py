@@ -305,6 +305,43 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(F, args):
+    """Only the chosen workload's step, args.warmup + args.steps times."""
+    name = args.profile
+    if name in ("c2", "c4", "c4causal", "c1"):
+        if name == "c1":
+            case, _ = W.config1()
+            case = W.PrefillCase("c1", case.q.to(torch.bfloat16), case.k.to(torch.bfloat16),
+                                 case.v.to(torch.bfloat16), True, case.scale)
+        else:
+            case = W.config2() if name == "c2" else W.config4()
+        q, k, v, out = prefill_setup(case)
+        if name == "c4":
+            M = case.mask.cuda()
+            wsb = torch.empty(F.fa_prefill_masked_workspace_size(case.T), dtype=torch.uint8, device="cuda")
+
+            def step():
+                F.fa_prefill_masked(q, k, v, M, causal=False, scale=case.scale, out=out, ws=wsb)
+        else:
+            def step():
+                F.fa_prefill(q, k, v, causal=True, scale=case.scale, out=out)
+    else:
+        p = W.config3() if name == "c3" else W.config5()
+        t = paged_setup(F, p)
+        max_q = int(p.q_lens.max())
+
+        def step():
+            F.fa_paged_attn(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["ql"], causal=p.causal, scale=p.scale,
+                            out=t["out"], max_q_len=max_q, ws=t["ws"])
+    for _ in range(args.warmup + args.steps):
+        step()
+    torch.cuda.synchronize()
+    st = F.fa_get_error()
+    print(f"profile {name}: {args.warmup + args.steps} steps, status {F.status_string(st)}", flush=True)
+    if st != F.FA_OK:
+        sys.exit(1)
+
+
 # -------------------------------------------------------------------- main ---
 def main():
     ap = argparse.ArgumentParser()
@@ -314,6 +351,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-warm-s", type=float, default=1.5,
+                    help="minimum warm-up time of the primary workload (clock sampling starts with it)")
+    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c4causal", "c5"], default=None,
+                    help="run only this workload's step (warm-up + steps, no L2 flush, no JSON) for ncu captures")
     args = ap.parse_args()
     ws, rank, local = dist_init()
     if args.impl == "reference":
@@ -325,6 +366,10 @@ def main():
     build.build()
     from paged_kv_cache_tiled_gb300 import fattn as F
 
+    if args.profile:
+        run_profile(F, args)
+        return
+
     peaks, peak_src = load_peaks()
     traffic = profile_traffic()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
@@ -333,7 +378,8 @@ def main():
 
     # ---------------- primary: config 2 prefill
     c2 = W.config2()
-    res = bench_prefill(F, timer, c2, args.steps, args.warmup, ws, peaks, sampler=sampler, min_warm_s=1.5)
+    res = bench_prefill(F, timer, c2, args.steps, args.warmup, ws, peaks, sampler=sampler,
+                        min_warm_s=args.min_warm_s)
     tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roof = {"bound": "tensor", "achieved": res["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
             "frac": res["tflops"] / tc_peak, "traffic": traffic.get("attn_tc_dense_c2"),

@@ -11,6 +11,7 @@ from fa_testutil import bits
 
 pytestmark = pytest.mark.gpu
 CANARY = 0xA5A5
+CANARY_I16 = CANARY - 0x10000  # same 16 bits as a signed value
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +23,7 @@ def F():
 
 
 def canary_cache(nb, Hkv, d):
-    return torch.full((nb, Hkv, 16, d), CANARY, dtype=torch.int16).view(torch.bfloat16).cuda()
+    return torch.full((nb, Hkv, 16, d), CANARY_I16, dtype=torch.int16).view(torch.bfloat16).cuda()
 
 
 def test_stage_bf16_matches_oracle_rounding(F):
@@ -80,7 +81,7 @@ def test_gather_random_tables(F):
                      fill_unused=0.5)
     ctx = p.ctx_lens
     max_ctx = int(ctx.max())
-    sentinel = torch.full((5, max_ctx, 2, 64), CANARY, dtype=torch.int16).view(torch.bfloat16).cuda()
+    sentinel = torch.full((5, max_ctx, 2, 64), CANARY_I16, dtype=torch.int16).view(torch.bfloat16).cuda()
     out = F.fa_debug_gather_kv(p.k_cache.cuda(), p.block_table.cuda(), ctx.cuda(), max_ctx, out=sentinel)
     assert F.fa_get_error() == F.FA_OK
     got = bits(out)
