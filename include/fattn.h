@@ -71,7 +71,8 @@ const char* fa_status_string(fa_status status);
  *   k,v bf16 [B, T, Hkv, d]
  *   out bf16 [B, T, Hq, d] (written; may not alias the inputs)
  *   lse fp32 [B, Hq, T] natural-log log-sum-exp of each row's scores, or NULL
- *   scale multiplies Q K^T (1/sqrt(d) for the textbook form)
+ *   scale multiplies Q K^T (1/sqrt(d) for the textbook form); must be finite
+ *         and > 0 (FA_ERR_INVALID_ARG otherwise)
  * Tq = Tk = T.  T may be any positive length (ragged final tile).
  */
 fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int B, int T,
@@ -136,6 +137,7 @@ fa_status fa_cache_append(const void* k, const void* v, void* k_cache, void* v_c
  *                a valid bound); used only to skip launching a kernel that
  *                would find no work
  *   block_size   must be 16
+ *   scale        finite and > 0, multiplies Q K^T
  *   ws           workspace of at least fa_paged_attn_workspace_size(...) bytes
  *                (split partials and scheduling lists); contents need not be
  *                initialised

@@ -36,6 +36,7 @@
 // the row sum stay consistent with a possibly stale max (exact up to
 // rounding); P is rounded to bf16 for the tensor core, row sums stay fp32.
 #include <algorithm>
+#include <cmath>
 
 #include "host_common.cuh"
 
@@ -75,6 +76,7 @@ struct TcParams {
     const float* mask;
     const uint8_t* cls;
     const int32_t* qt_order;
+    const int2* qt_range;  // per query tile: [first, last+1) of its KV tiles that are not all -inf
     // paged
     const int32_t* bt;
     const int32_t* ctx_lens;
@@ -95,7 +97,8 @@ struct Unit {
     int qtok[2];    // row coordinate for the Q tile load
     int kv_len;     // keys of the sequence (T or ctx)
     int pos_off;    // key position of query row i is i + pos_off
-    int n_kt;       // KV tiles to scan
+    int kt0;        // first KV tile to scan
+    int n_kt;       // KV tiles to scan: [kt0, n_kt)
 };
 
 // i-th unit of this CTA: units are ordered longest first and dealt to the CTAs
@@ -137,6 +140,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
         U.kv_len = cl;
         U.pos_off = cl - ql;
         const int kv_end = p.causal ? min(cl, cl - ql + last) : cl;
+        U.kt0 = 0;
         U.n_kt = (kv_end + kTcRows - 1) / kTcRows;
     } else {
         const int nqt = (p.T + kTcRows - 1) / kTcRows;
@@ -176,7 +180,21 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
         U.kv_len = p.T;
         U.pos_off = 0;
         const int kv_end = p.causal ? last : p.T;
+        U.kt0 = 0;
         U.n_kt = (kv_end + kTcRows - 1) / kTcRows;
+        if constexpr (MODE == MODE_MASKED) {
+            // restrict the scan to the KV tiles the mask leaves visible
+            int lo = U.n_kt, hi = 0;
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+                if (U.nrows[s] > 0) {
+                    const int2 r = __ldg(p.qt_range + U.row0[s] / kTcRows);
+                    lo = min(lo, r.x);
+                    hi = max(hi, r.y);
+                }
+            U.kt0 = lo;
+            U.n_kt = min(U.n_kt, hi);
+        }
     }
     return U;
 }
@@ -203,13 +221,8 @@ __device__ __forceinline__ bool skip_tile(const TcParams& p, const Unit& U, int 
 
 template <int MODE>
 __device__ __forceinline__ bool unit_active(const TcParams& p, const Unit& U) {
-    if (U.n_kt <= 0) return false;
-    if constexpr (MODE == MODE_MASKED) {
-        for (int kt = 0; kt < U.n_kt; ++kt)
-            if (!skip_tile<MODE>(p, U, kt)) return true;
-        return false;
-    }
-    return true;
+    (void)p;
+    return U.kt0 < U.n_kt;  // in masked mode [kt0, n_kt) starts and ends on a visible tile
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -310,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (!ok) break;
             ++qcnt;
-            for (int kt = 0; kt < U.n_kt && ok; ++kt) {
+            for (int kt = U.kt0; kt < U.n_kt && ok; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
                 for (int which = 0; which < 2; ++which) {  // 0: K tile, 1: V tile
                     const int stage = fill % S;
@@ -422,7 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) break;
             ++ucnt;
             int it = 0, prev_v = -1, prev_kt = -1;
-            for (int kt = 0; kt < U.n_kt && ok; ++kt) {
+            for (int kt = U.kt0; kt < U.n_kt && ok; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
                 const int kidx = cons + 2 * it;
                 if (!mbar_wait_warp(&full[kidx % S], (kidx / S) & 1, lim_ns, abort_flag)) {
@@ -528,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int vis_end = p.causal ? min(U.kv_len, row + U.pos_off + 1) : U.kv_len;
             float m = -INFINITY, l = 0.f;
             int it = 0;
-            for (int kt = 0; kt < U.n_kt; ++kt) {
+            for (int kt = U.kt0; kt < U.n_kt; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
                 if (!mbar_wait_warp(&sfull[s], sc & 1, lim_ns, abort_flag)) {
                     ok = false;
@@ -540,22 +553,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int lim = vis_end - kv0;  // visible columns of this tile: [0, lim)
                 const int cls = tile_class<MODE>(p, U, s, kt);
                 const float* mrow = (cls == 2 && valid) ? p.mask + (long)row * p.T + kv0 : nullptr;
-                // scaled, masked score of column j (base-2 logits)
+                // every column visible and no mask values to add: scores only need the scale
+                const bool plain = (cls == 1) && (lim >= kTcRows);
+                // scaled, masked score of column j (base-2 logits), general case
                 auto logit = [&](float sv, int j) -> float {
                     if (cls == 0 || j >= lim) return -INFINITY;
                     if (mrow) return fmaf(sv, p.scale_log2, __ldg(mrow + j) * kLog2e);
                     return sv * p.scale_log2;
                 };
-                // pass 1: row max, 32 columns at a time
+                // pass 1: row max, 64 columns per TMEM wait (scale > 0, so the
+                // max of the raw scores gives the max of the scaled ones)
                 float mx = -INFINITY;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(trow + s_col + c * 32, raw);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t raw[64];
+                    tmem_ld32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+                    tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     tmem_wait_ld();
+                    if (plain) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, logit(__uint_as_float(raw[j]), c * 32 + j));
+                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, __uint_as_float(raw[j]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, logit(__uint_as_float(raw[j]), h * 64 + j));
+                    }
                 }
+                if (plain) mx *= p.scale_log2;
                 const float m_new = fmaxf(m, mx);
                 const bool need = m_new > m + kRescaleThreshold;
                 float alpha = 1.f;
@@ -567,23 +590,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const float m_use = (m == -INFINITY) ? 0.f : m;
                 // pass 2: P = 2^(logit - m) as bf16 into the first 64 columns of S.
-                // Chunk c reads S columns [32c, 32c+32) and writes P columns
-                // [16c, 16c+16), which only overlap S columns already read.
+                // Half h reads S columns [64h, 64h+64) and writes P columns
+                // [32h, 32h+32), which only overlap S columns already read.
                 float rs = 0.f;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t raw[32];
-                    tmem_ld32(trow + s_col + c * 32, raw);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t raw[64];
+                    tmem_ld32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+                    tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     tmem_wait_ld();
-                    uint32_t pk[16];
+                    uint32_t pk[32];
+                    if (plain) {
+                        const float neg_m = -m_use;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float p0 = fast_exp2(logit(__uint_as_float(raw[2 * j]), c * 32 + 2 * j) - m_use);
-                        const float p1 = fast_exp2(logit(__uint_as_float(raw[2 * j + 1]), c * 32 + 2 * j + 1) - m_use);
-                        rs += p0 + p1;
-                        pk[j] = pack_bf16x2(p0, p1);
+                        for (int j = 0; j < 32; ++j) {
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(raw[2 * j]), p.scale_log2, neg_m));
+                            const float p1 = fast_exp2(fmaf(__uint_as_float(raw[2 * j + 1]), p.scale_log2, neg_m));
+                            rs += p0 + p1;
+                            pk[j] = pack_bf16x2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float p0 = fast_exp2(logit(__uint_as_float(raw[2 * j]), h * 64 + 2 * j) - m_use);
+                            const float p1 =
+                                fast_exp2(logit(__uint_as_float(raw[2 * j + 1]), h * 64 + 2 * j + 1) - m_use);
+                            rs += p0 + p1;
+                            pk[j] = pack_bf16x2(p0, p1);
+                        }
                     }
-                    tmem_st16(trow + s_col + c * 16, pk);
+                    tmem_st32(trow + s_col + h * 32, pk);
                 }
                 l += rs;
                 if (warp_rescale && it > 0) {
@@ -642,13 +678,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Orders query tiles by decreasing number of KV tiles that are not entirely
 // masked (longest first), from the tile classes of the additive mask.
 __global__ void __launch_bounds__(256) mask_order_kernel(const uint8_t* __restrict__ cls, int nqt, int nkt,
-                                                         int causal, int32_t* __restrict__ order) {
+                                                         int causal, int32_t* __restrict__ order,
+                                                         int2* __restrict__ range) {
     extern __shared__ int cost[];
     for (int q = threadIdx.x; q < nqt; q += blockDim.x) {
-        int c = 0;
+        int c = 0, lo = nkt, hi = 0;
         const int kend = causal ? min(nkt, q + 1) : nkt;
-        for (int k = 0; k < kend; ++k) c += cls[(long)q * nkt + k] != 0;
+        for (int k = 0; k < kend; ++k)
+            if (cls[(long)q * nkt + k] != 0) {
+                ++c;
+                lo = min(lo, k);
+                hi = k + 1;
+            }
         cost[q] = c;
+        range[q] = make_int2(lo, hi);
     }
     __syncthreads();
     for (int q = threadIdx.x; q < nqt; q += blockDim.x) {
@@ -696,8 +739,8 @@ static fa_status dense_maps(const void* q, const void* k, const void* v, int B, 
 }
 
 static fa_status check_prefill_args(const void* q, const void* k, const void* v, const void* out, int B, int T,
-                                    int Hq, int Hkv, int d) {
-    if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0) return FA_ERR_INVALID_ARG;
+                                    int Hq, int Hkv, int d, float scale) {
+    if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || !(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if ((d != 64 && d != 128) || Hq % Hkv != 0) return FA_ERR_UNSUPPORTED;
     if (B == 0 || T == 0) return FA_OK;
     if (!q || !k || !v || !out) return FA_ERR_INVALID_ARG;
@@ -765,7 +808,7 @@ extern "C" {
 fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv, int d,
                      int causal, float scale, float* lse, fa_stream_t stream) {
     set_launch_count(0);
-    fa_status st = check_prefill_args(q, k, v, out, B, T, Hq, Hkv, d);
+    fa_status st = check_prefill_args(q, k, v, out, B, T, Hq, Hkv, d, scale);
     if (st != FA_OK || B == 0 || T == 0) return st;
     if ((st = check_device()) != FA_OK) return st;
     DevCtx ctx;
@@ -783,14 +826,14 @@ fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int
 size_t fa_prefill_masked_workspace_size(int T) {
     if (T <= 0) return 0;
     const size_t nt = (size_t)(T + kTcRows - 1) / kTcRows;
-    return align256(nt * nt) + align256(sizeof(int32_t) * nt);
+    return align256(nt * nt) + align256(sizeof(int32_t) * nt) + align256(sizeof(int2) * nt);
 }
 
 fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const float* mask, void* out, int B, int T,
                             int Hq, int Hkv, int d, int causal, float scale, float* lse, void* ws, size_t ws_bytes,
                             fa_stream_t stream) {
     set_launch_count(0);
-    fa_status st = check_prefill_args(q, k, v, out, B, T, Hq, Hkv, d);
+    fa_status st = check_prefill_args(q, k, v, out, B, T, Hq, Hkv, d, scale);
     if (st != FA_OK || B == 0 || T == 0) return st;
     if (!mask) return fa_prefill(q, k, v, out, B, T, Hq, Hkv, d, causal, scale, lse, stream);
     if (!ws || ws_bytes < fa_prefill_masked_workspace_size(T) || (reinterpret_cast<uintptr_t>(ws) & 255))
@@ -804,18 +847,21 @@ fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const f
     const int nt = (T + kTcRows - 1) / kTcRows;
     uint8_t* cls = static_cast<uint8_t*>(ws);
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + align256((size_t)nt * nt));
+    int2* range = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + align256((size_t)nt * nt) +
+                                          align256(sizeof(int32_t) * nt));
     if ((st = launch_mask_classify(mask, T, T, cls, s)) != FA_OK) return st;
     if ((size_t)nt * sizeof(int) > 200 * 1024) return FA_ERR_UNSUPPORTED;
     if (nt * sizeof(int) > 48 * 1024 &&
         cudaFuncSetAttribute(mask_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, nt * (int)sizeof(int)) !=
             cudaSuccess)
         return FA_ERR_CUDA;
-    mask_order_kernel<<<1, 256, nt * sizeof(int), s>>>(cls, nt, nt, causal ? 1 : 0, order);
+    mask_order_kernel<<<1, 256, nt * sizeof(int), s>>>(cls, nt, nt, causal ? 1 : 0, order, range);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     TcParams p = base_params(B, T, Hq, Hkv, causal, scale, out, lse, ctx);
     p.mask = mask;
     p.cls = cls;
     p.qt_order = order;
+    p.qt_range = range;
     p.num_units = dense_units(p);
     const int grid = std::min(p.num_units, sm_count());
     st = launch_tc_d<MODE_MASKED>(d, tq, tk, tv, p, grid, s);

@@ -531,7 +531,7 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
                         float scale, int total_q, int max_q_len, void* ws, size_t ws_bytes, fa_stream_t stream) {
     set_launch_count(0);
     if (num_seqs < 0 || max_blocks_per_seq < 0 || num_blocks < 0 || Hq <= 0 || Hkv <= 0 || total_q < 0 ||
-        max_q_len < 0)
+        max_q_len < 0 || !(scale > 0.f) || !(scale < INFINITY))
         return FA_ERR_INVALID_ARG;
     if (block_size != kBS || (d != 64 && d != 128) || Hq % Hkv != 0) return FA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return FA_OK;
