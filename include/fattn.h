@@ -155,6 +155,40 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
                         fa_stream_t stream);
 
 /*
+ * fa_paged_attn_noalloc -- fa_paged_attn for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is a convenience of the
+ * library, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc: a process whose device memory was
+ * reserved up front by another runtime's pool (a fresh allocation would fail
+ * or fragment that pool), or a plugin interface that hands over inputs and
+ * outputs but no scratch space.  This entry point takes the same arguments as
+ * fa_paged_attn minus the workspace and uses instead a fixed scratch array of
+ * FA_NOALLOC_SCRATCH_BYTES (16 MiB) that the library keeps on every GPU that
+ * loads it, until the process exits.  It calls no allocator.
+ *   - Problems whose fa_paged_attn_workspace_size(...) exceeds
+ *     FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE before any
+ *     launch (the decode partials grow with num_seqs * Hkv * splits * d).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents.  Nothing in it has to start at zero: each call writes what it
+ *     later reads.  Calls that overlap on the GPU (different streams, or
+ *     different host threads without ordering) race on it and must not be
+ *     issued.
+ * Everything else -- arguments, layouts, results, errors -- is as for
+ * fa_paged_attn.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+fa_status fa_paged_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* ctx_lens,
+                                const int32_t* q_lens, void* out, int num_seqs,
+                                int max_blocks_per_seq, int num_blocks, int Hq, int Hkv, int d,
+                                int block_size, int causal, float scale, int total_q,
+                                int max_q_len, fa_stream_t stream);
+
+/*
  * fa_get_error -- synchronises `stream`, then returns and clears the current
  * device's error word: FA_OK, FA_ERR_BOUNDS or FA_ERR_TIMEOUT (FA_ERR_BOUNDS
  * when both were recorded), or FA_ERR_CUDA if synchronisation itself failed.

@@ -24,6 +24,8 @@
 //     with log-sum-exp weights.
 // Longer chunks take the tensor-core kernel (attn_tc.cu) through a work list
 // built on the device by `paged_meta_kernel`.
+#include <mutex>
+
 #include "host_common.cuh"
 
 namespace fa {
@@ -582,3 +584,44 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------ allocation-free ---
+// Scratch for fa_paged_attn_noalloc: a fixed device array that every GPU
+// loading this library holds until the process exits.  Host code only sees a
+// stand-in for its name, so its device address is looked up per device with
+// cudaGetSymbolAddress (with that device current) and handed to the kernels.
+namespace fa {
+namespace {
+static __device__ __align__(256) uint8_t g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+fa_status noalloc_scratch(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FA_OK;
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_paged_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* block_table, const int32_t* ctx_lens,
+                                           const int32_t* q_lens, void* out, int num_seqs, int max_blocks_per_seq,
+                                           int num_blocks, int Hq, int Hkv, int d, int block_size, int causal,
+                                           float scale, int total_q, int max_q_len, fa_stream_t stream) {
+    const size_t need = fa_paged_attn_workspace_size(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q);
+    if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;  // problem too large for the fixed scratch
+    void* scratch = nullptr;
+    fa_status st = fa::noalloc_scratch(&scratch);
+    if (st != FA_OK) return st;
+    return fa_paged_attn(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, num_seqs, max_blocks_per_seq,
+                         num_blocks, Hq, Hkv, d, block_size, causal, scale, total_q, max_q_len, scratch,
+                         FA_NOALLOC_SCRATCH_BYTES, stream);
+}

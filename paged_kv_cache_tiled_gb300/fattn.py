@@ -24,8 +24,9 @@ FA_BF16, FA_F32 = 0, 1
 EXPORTS = [
     "fa_status_string", "fa_prefill", "fa_prefill_masked_workspace_size", "fa_prefill_masked", "fa_stage_bf16",
     "fa_cache_append", "fa_paged_attn_workspace_size", "fa_paged_attn", "fa_get_error", "fa_debug_gather_kv",
-    "fa_debug_set_wait_limit", "fa_debug_force_timeout", "fa_last_launch_count",
+    "fa_debug_set_wait_limit", "fa_debug_force_timeout", "fa_last_launch_count", "fa_paged_attn_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 16 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
 
 class FattnError(RuntimeError):
@@ -53,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "fa_debug_gather_kv": (I, [P, P, P, P, I, I, I, I, I, I, P]),
         "fa_debug_set_wait_limit": (None, [ctypes.c_ulonglong]),
         "fa_debug_force_timeout": (None, [I]),
+        "fa_paged_attn_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P]),
         "fa_last_launch_count": (I, []),
     }
     for name, (res, args) in sig.items():
@@ -201,6 +203,33 @@ def fa_paged_attn(q, k_cache, v_cache, block_table, ctx_lens, q_lens, causal: bo
                               _ptr(q_lens), _ptr(out), num_seqs, mbps, num_blocks, Hq, Hkv, d, bs, int(causal),
                               float(scale), total_q, int(max_q_len), _ptr(ws), ws.numel() * ws.element_size(),
                               _stream(stream)), "fa_paged_attn")
+    return out
+
+
+def fa_paged_attn_noalloc(q, k_cache, v_cache, block_table, ctx_lens, q_lens, causal: bool = True,
+                          scale: float | None = None, out=None, max_q_len: int | None = None, stream=None):
+    """fa_paged_attn without a workspace, for callers that cannot allocate device
+    scratch: the library's fixed 16 MiB per-device array is used instead.  Calls
+    must not overlap on the GPU (they share that array)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    _need(q_lens, "q_lens", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    num_blocks, Hkv, bs, _ = k_cache.shape
+    num_seqs, mbps = block_table.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if max_q_len is None:
+        max_q_len = total_q
+    _check(_lib.fa_paged_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens),
+                                      _ptr(q_lens), _ptr(out), num_seqs, mbps, num_blocks, Hq, Hkv, d, bs,
+                                      int(causal), float(scale), total_q, int(max_q_len), _stream(stream)),
+           "fa_paged_attn_noalloc")
     return out
 
 
