@@ -190,7 +190,10 @@ def prefill_setup(case):
     return q, k, v, out
 
 
-def bench_prefill(F, timer, case, steps, warmup, ws, peaks, sampler=None, masked=False, min_warm_s=0.0):
+def bench_prefill(F, timer, case, steps, warmup, ws, peaks, sampler=None, masked=False, min_warm_s=0.0,
+                  causal=None):
+    """`causal` overrides the case's flag (config 4 carries its causality in M)."""
+    causal = case.causal if causal is None else causal
     q, k, v, out = prefill_setup(case)
     flops = W.attention_flops(case.T, case.T, case.d, case.B * case.Hq, True)
     if masked:
@@ -201,7 +204,7 @@ def bench_prefill(F, timer, case, steps, warmup, ws, peaks, sampler=None, masked
             F.fa_prefill_masked(q, k, v, M, causal=False, scale=case.scale, out=out, ws=wsb)
     else:
         def step():
-            F.fa_prefill(q, k, v, causal=case.causal, scale=case.scale, out=out)
+            F.fa_prefill(q, k, v, causal=causal, scale=case.scale, out=out)
     if sampler:
         sampler.start()
     ms, launches, wall, _ = timer.run(step, steps, warmup, ws, min_warm_s=min_warm_s)
@@ -433,7 +436,7 @@ def main():
         steps4 = max(3, min(args.steps, 10))
         c4 = W.config4()
         r4 = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks, masked=True)
-        r4c = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks)
+        r4c = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks, causal=True)
         for r, name in ((r4, "additive mask M (-inf above diagonal) via fa_prefill_masked"),
                         (r4c, "causal flag via fa_prefill")):
             sec.append({"workload": f"config 4: long prefill B=1 T=16384 Hq=32 Hkv=8 d=128, {name}",

@@ -58,7 +58,7 @@ struct TcCfg {
     static constexpr int kStages = D == 128 ? 4 : 8;
     static constexpr int kQBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kStages * kTileBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * 5 + 2;
+    static constexpr int kNumBars = 2 * kStages + 2 * 6 + 2;
     static constexpr int kSmem = 1024 + kQBytes + kRingBytes + kNumBars * 8 + 16;
     static constexpr uint32_t kS0 = 0, kS1 = 128, kO0 = 256, kO1 = 256 + D;
 };
@@ -225,6 +225,24 @@ __device__ __forceinline__ bool unit_active(const TcParams& p, const Unit& U) {
     return U.kt0 < U.n_kt;  // in masked mode [kt0, n_kt) starts and ends on a visible tile
 }
 
+// Output row r of slot s of a unit (bf16, d channels).
+template <int D, int MODE>
+__device__ __forceinline__ uint16_t* out_row(const TcParams& p, const Unit& U, int s, int r) {
+    if constexpr (MODE == MODE_PAGED)
+        return p.out + ((long)U.qtok[s] + r) * p.Hq * D + (long)U.head[s] * D;
+    else
+        return p.out + (((long)U.b * p.T + U.row0[s] + r) * p.Hq + U.head[s]) * D;
+}
+
+// A row that sees no key: output 0, LSE -inf.
+template <int D, int MODE>
+__device__ __noinline__ void store_zero_row(const TcParams& p, const Unit& U, int s, int r) {
+    uint16_t* orow = out_row<D, MODE>(p, U, s, r);
+    for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+    if constexpr (MODE != MODE_PAGED)
+        if (p.lse) p.lse[((long)U.b * p.Hq + U.head[s]) * p.T + U.row0[s] + r] = -INFINITY;
+}
+
 // ------------------------------------------------------------------ kernel --
 template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -241,8 +259,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* qfull = empty + S;
     uint64_t* qempty = qfull + 2;
     uint64_t* sfull = qempty + 2;
-    uint64_t* pfull = sfull + 2;
-    uint64_t* ofull = pfull + 2;
+    uint64_t* pfull = sfull + 2;  // [slot * 2 + half]: P columns of that half written (and O rescaled)
+    uint64_t* ofull = pfull + 4;
     uint64_t* drain = ofull + 2;
     uint64_t* never = drain + 1;  // nothing arrives on it (forced time-out test hook)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
@@ -258,7 +276,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&qfull[s], 1);
             mbar_init(&qempty[s], 1);
             mbar_init(&sfull[s], 1);
-            mbar_init(&pfull[s], kTcRows);
+            mbar_init(&pfull[2 * s], kTcRows);
+            mbar_init(&pfull[2 * s + 1], kTcRows);
             mbar_init(&ofull[s], 1);
         }
         mbar_init(drain, 1);
@@ -416,12 +435,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         kIdescQK, kk > 0);
             }
         };
-        auto issue_pv = [&](int s, int vidx, bool acc_first) {
+        // O_s += P_s V over keys [64h, 64h+64) of the tile
+        auto issue_pv_half = [&](int s, int vidx, int h, bool acc_first) {
             const uint32_t vb = ring_addr + (vidx % S) * C::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < kTcRows / 16; ++kk)
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int kk = 4 * h + k4;
                 umma_ts(tbase + o_col[s], tbase + s_col[s] + kk * 8,
                         smem_desc_sw128(vb + kk * 2048, C::kAtomBytes, 1024), kIdescPV, (acc_first || kk > 0));
+            }
+        };
+        // waits for each half of P_s in turn and issues its P*V MMAs
+        auto pv = [&](int s, int vidx, bool acc_first) -> bool {
+            for (int h = 0; h < 2; ++h) {
+                if (!mbar_wait_warp(&pfull[2 * s + h], pc[s] & 1, lim_ns, abort_flag)) return false;
+                tc_fence_after();
+                if (lane == 0) issue_pv_half(s, vidx, h, acc_first);
+                __syncwarp();
+            }
+            ++pc[s];
+            return true;
         };
 
         for (int i = 0; ok; ++i) {
@@ -449,13 +482,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             ok = false;
                             break;
                         }
-                        if (!mbar_wait_warp(&pfull[s], pc[s] & 1, lim_ns, abort_flag)) {
+                        if (!pv(s, prev_v, it > 1)) {
                             ok = false;
                             break;
                         }
-                        ++pc[s];
-                        tc_fence_after();
-                        if (lane == 0) issue_pv(s, prev_v, it > 1);
                     }
                     if (lane == 0) {
                         issue_qk(s, kidx);
@@ -483,16 +513,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             for (int s = 0; s < 2 && ok; ++s) {
-                if (!mbar_wait_warp(&pfull[s], pc[s] & 1, lim_ns, abort_flag)) {
+                if (!pv(s, prev_v, it > 1)) {
                     ok = false;
                     break;
                 }
-                ++pc[s];
-                tc_fence_after();
-                if (lane == 0) {
-                    issue_pv(s, prev_v, it > 1);
-                    umma_commit(&ofull[s]);
-                }
+                if (lane == 0) umma_commit(&ofull[s]);
                 __syncwarp();
             }
             if (!ok) break;
@@ -522,19 +547,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const Unit U = decode_unit<MODE>(p, u);
             const bool valid = r < U.nrows[s];
             const int row = U.row0[s] + r;  // row within T (dense) or within the chunk (paged)
-            uint16_t* orow;
-            if constexpr (MODE == MODE_PAGED)
-                orow = p.out + ((long)U.qtok[s] + r) * p.Hq * D + (long)U.head[s] * D;
-            else
-                orow = p.out + (((long)U.b * p.T + row) * p.Hq + U.head[s]) * D;
-            float* lse_ptr = nullptr;
-            if constexpr (MODE != MODE_PAGED)
-                if (p.lse && valid) lse_ptr = p.lse + ((long)U.b * p.Hq + U.head[s]) * p.T + row;
             if (!unit_active<MODE>(p, U)) {
-                if (valid) {
-                    for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-                    if (lse_ptr) *lse_ptr = -INFINITY;
-                }
+                if (valid) store_zero_row<D, MODE>(p, U, s, r);
                 continue;
             }
             // key j is visible when j <= row + pos_off (causal) and j < kv_len
@@ -553,32 +567,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int lim = vis_end - kv0;  // visible columns of this tile: [0, lim)
                 const int cls = tile_class<MODE>(p, U, s, kt);
                 const float* mrow = (cls == 2 && valid) ? p.mask + (long)row * p.T + kv0 : nullptr;
-                // every column visible and no mask values to add: scores only need the scale
-                const bool plain = (cls == 1) && (lim >= kTcRows);
-                // scaled, masked score of column j (base-2 logits), general case
-                auto logit = [&](float sv, int j) -> float {
-                    if (cls == 0 || j >= lim) return -INFINITY;
-                    if (mrow) return fmaf(sv, p.scale_log2, __ldg(mrow + j) * kLog2e);
-                    return sv * p.scale_log2;
-                };
-                // pass 1: row max, 64 columns per TMEM wait (scale > 0, so the
-                // max of the raw scores gives the max of the scaled ones)
+                // every column visible and no mask values to add: scores only need the
+                // scale.  Decided per warp (the general path also covers plain rows),
+                // because the general path issues warp-collective TMEM stores.
+                const bool plain = !__any_sync(0xffffffffu, !((cls == 1) && (lim >= kTcRows)));
+                // pass 1: row max, 64 columns per TMEM wait.  In the general case
+                // the masked, scaled logits are written back over S so that pass
+                // 2 reads them instead of re-reading the mask.
                 float mx = -INFINITY;
+                const bool vec_mask = mrow && ((p.T & 3) == 0);
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     uint32_t raw[64];
                     tmem_ld32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
                     tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     tmem_wait_ld();
-                    if (plain) {
+                    if (plain) {  // scale > 0: the max of the raw scores gives the max of the scaled ones
 #pragma unroll
                         for (int j = 0; j < 64; ++j) mx = fmaxf(mx, __uint_as_float(raw[j]));
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, logit(__uint_as_float(raw[j]), h * 64 + j));
+                        for (int j4 = 0; j4 < 16; ++j4) {
+                            float mv[4] = {0.f, 0.f, 0.f, 0.f};
+                            const int j0 = h * 64 + 4 * j4;
+                            if (vec_mask && j0 + 3 < lim) {
+                                const float4 t = __ldg(reinterpret_cast<const float4*>(mrow + j0));
+                                mv[0] = t.x; mv[1] = t.y; mv[2] = t.z; mv[3] = t.w;
+                            } else if (mrow) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) mv[e] = (j0 + e < lim) ? __ldg(mrow + j0 + e) : 0.f;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = j0 + e;
+                                const float x = (cls == 0 || j >= lim)
+                                                    ? -INFINITY
+                                                    : fmaf(__uint_as_float(raw[4 * j4 + e]), p.scale_log2, mv[e] * kLog2e);
+                                raw[4 * j4 + e] = __float_as_uint(x);
+                                mx = fmaxf(mx, x);
+                            }
+                        }
+                        tmem_st32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+                        tmem_st32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     }
                 }
                 if (plain) mx *= p.scale_log2;
+                else tmem_wait_st();
                 const float m_new = fmaxf(m, mx);
                 const bool need = m_new > m + kRescaleThreshold;
                 float alpha = 1.f;
@@ -589,9 +623,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     m = m_new;
                 }
                 const float m_use = (m == -INFINITY) ? 0.f : m;
-                // pass 2: P = 2^(logit - m) as bf16 into the first 64 columns of S.
-                // Half h reads S columns [64h, 64h+64) and writes P columns
-                // [32h, 32h+32), which only overlap S columns already read.
+                // O must be rescaled before the first P*V of this tile: in that
+                // (rare) case both halves are signalled after the rescale
+                const bool rescale_o = warp_rescale && it > 0;
+                // pass 2: P = 2^(logit - m) as bf16.  Half h reads S columns
+                // [64h, 64h+64) and writes P columns [32h, 32h+32), only over S
+                // columns already read.
                 float rs = 0.f;
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
@@ -600,42 +637,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     tmem_wait_ld();
                     uint32_t pk[32];
-                    if (plain) {
-                        const float neg_m = -m_use;
+                    const float sc2 = plain ? p.scale_log2 : 1.f;  // logits already scaled in the general case
+                    const float neg_m = -m_use;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float p0 = fast_exp2(fmaf(__uint_as_float(raw[2 * j]), p.scale_log2, neg_m));
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(raw[2 * j + 1]), p.scale_log2, neg_m));
-                            rs += p0 + p1;
-                            pk[j] = pack_bf16x2(p0, p1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float p0 = fast_exp2(logit(__uint_as_float(raw[2 * j]), h * 64 + 2 * j) - m_use);
-                            const float p1 =
-                                fast_exp2(logit(__uint_as_float(raw[2 * j + 1]), h * 64 + 2 * j + 1) - m_use);
-                            rs += p0 + p1;
-                            pk[j] = pack_bf16x2(p0, p1);
-                        }
+                    for (int j = 0; j < 32; ++j) {
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(raw[2 * j]), sc2, neg_m));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(raw[2 * j + 1]), sc2, neg_m));
+                        rs += p0 + p1;
+                        pk[j] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(trow + s_col + h * 32, pk);
                 }
+                if (!rescale_o) {  // P complete: hand the tile to the MMA warp
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&pfull[2 * s]);
+                    mbar_arrive(&pfull[2 * s + 1]);
+                }
                 l += rs;
-                if (warp_rescale && it > 0) {
-#pragma unroll
+                if (rescale_o) {
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
-                        uint32_t raw[32];
-                        tmem_ld32(trow + o_col + c * 32, raw);
+                        uint32_t o[32];
+                        tmem_ld32(trow + o_col + c * 32, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) raw[j] = __float_as_uint(__uint_as_float(raw[j]) * alpha);
-                        tmem_st32(trow + o_col + c * 32, raw);
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tmem_st32(trow + o_col + c * 32, o);
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&pfull[2 * s]);
+                    mbar_arrive(&pfull[2 * s + 1]);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&pfull[s]);
                 ++it;
             }
             if (!ok) break;
@@ -645,6 +679,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             ++oc;
             tc_fence_after();
+            const Unit E = decode_unit<MODE>(p, u);  // re-derived here so its fields are not live across the tile loop
+            uint16_t* orow = out_row<D, MODE>(p, E, s, r);
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -663,7 +699,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
                 }
             }
-            if (lse_ptr) *lse_ptr = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            if constexpr (MODE != MODE_PAGED)
+                if (p.lse && valid)
+                    p.lse[((long)E.b * p.Hq + E.head[s]) * p.T + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         }
         if (!ok && lane == 0) fail();
     }

@@ -24,6 +24,7 @@
 //     with log-sum-exp weights.
 // Longer chunks take the tensor-core kernel (attn_tc.cu) through a work list
 // built on the device by `paged_meta_kernel`.
+#include <cstdlib>
 #include <mutex>
 
 #include "host_common.cuh"
@@ -50,9 +51,16 @@ struct PagedWs {
     int split_blocks, max_splits, max_entries;
 };
 
+// Blocks per decode split (per CTA).  FA_DECODE_SPLIT_BLOCKS (8..256) overrides
+// the default for tuning; the workspace size query uses the same value.
 inline int decode_split_blocks(int mbps) {
     (void)mbps;
-    return 32;
+    static const int v = [] {
+        const char* e = getenv("FA_DECODE_SPLIT_BLOCKS");
+        const int x = e ? atoi(e) : 0;
+        return (x >= 8 && x <= 256) ? x : 64;
+    }();
+    return v;
 }
 
 inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, int total_q) {
@@ -120,6 +128,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     int* red = reinterpret_cast<int*>(never + 1);
     volatile int* abort_flag = red + 8;
 
+    // the merge kernel that follows may be scheduled now; it waits for this
+    // grid's completion before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int sp = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
     const int g = Hq / Hkv;
     const int q_len = __ldg(q_lens + s), ctx_len = __ldg(ctx_lens + s);
@@ -131,7 +142,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     const int nblk = (ctx_len + kBS - 1) / kBS;
     const int nsplit = (nblk + split_blocks - 1) / split_blocks;
     if (sp >= nsplit) return;
-    const int q0 = cta_prefix(q_lens, s, red);
     const int blk0 = sp * split_blocks, blk1 = min(nblk, blk0 + split_blocks);
     const int nrows = g * q_len;
 
@@ -172,6 +182,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     int issued = 0;  // lane 0's count of copies issued
     if (lane == 0 && ok)
         for (; issued < n_mine && issued < kDecodeStages; ++issued) issue(issued);
+    // the first copies are in flight; the query offset is computed meanwhile
+    const int q0 = cta_prefix(q_lens, s, red);
 
     // Q fragments (A operand, rows r = token * g + head-in-group)
     const int gid = lane >> 2, tig = lane & 3;
@@ -261,12 +273,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         }
         l0 = l0 * a0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
         l1 = l1 * a1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-            o[n][0] *= a0;
-            o[n][1] *= a0;
-            o[n][2] *= a1;
-            o[n][3] *= a1;
+            for (int n = 0; n < D / 8; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
         }
         uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(p[0][2], p[0][3]),
                           pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(p[1][2], p[1][3])};
@@ -351,39 +365,86 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 
 // Merges split partials: m = max_s m_s, l = sum_s 2^(m_s - m) l_s,
 // O = sum_s 2^(m_s - m) O_s / l  (O_s unnormalised, all in base 2).
+// One warp per row (8 warps, rows strided), lane j owns channels 4j..4j+3 and
+// split j's statistics, so every load of a row is issued at once.  Launched as
+// a programmatic dependent of the decode kernel: it may start early and waits
+// for that grid's results with griddepcontrol.wait.
+constexpr int kMergeThreads = 256;
 template <int D>
-__global__ void __launch_bounds__(128) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
-                                                          const int32_t* __restrict__ q_lens,
-                                                          const float* __restrict__ part_o,
-                                                          const float2* __restrict__ part_ml,
-                                                          uint16_t* __restrict__ out, int Hq, int Hkv,
-                                                          int split_blocks, int max_splits, int mbps) {
-    __shared__ int red[8];
+__global__ void __launch_bounds__(kMergeThreads) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
+                                                                    const int32_t* __restrict__ q_lens,
+                                                                    const float* __restrict__ part_o,
+                                                                    const float2* __restrict__ part_ml,
+                                                                    uint16_t* __restrict__ out, int Hq, int Hkv,
+                                                                    int split_blocks, int max_splits, int mbps) {
+    __shared__ int red[kMergeThreads / 32];
     const int s = blockIdx.x, hk = blockIdx.y, g = Hq / Hkv;
     const int q_len = __ldg(q_lens + s), ctx_len = __ldg(ctx_lens + s);
-    if (!is_decode_row(q_len, g) || q_len > ctx_len || ctx_len > mbps * kBS) return;
+    const bool active = is_decode_row(q_len, g) && q_len <= ctx_len && ctx_len <= mbps * kBS;
     const int nblk = (ctx_len + kBS - 1) / kBS;
     const int nsplit = (nblk + split_blocks - 1) / split_blocks;
-    if (nsplit <= 1) return;
-    const int q0 = cta_prefix(q_lens, s, red);
+    if (!active || nsplit <= 1) {
+        // even a CTA with nothing to do waits for the decode grid, so this grid
+        // never completes ahead of the one it depends on
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
+    const int q0 = cta_prefix(q_lens, s, red);  // inputs only: no need to wait for the decode grid yet
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int nrows = g * q_len;
     const long base = ((long)s * Hkv + hk) * max_splits;
-    const int per = blockDim.x / D > 0 ? blockDim.x / D : 1;
-    const int c = threadIdx.x % D;
-    for (int r = threadIdx.x / D; r < nrows; r += per) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kPer = D / 32;  // channels per lane
+    for (int r = warp; r < nrows; r += kMergeThreads / 32) {
         float M = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, part_ml[(base + sp) * kDecodeRows + r].x);
-        float acc = 0.f, lsum = 0.f;
-        if (M != -INFINITY)
-            for (int sp = 0; sp < nsplit; ++sp) {
-                const float2 ml = part_ml[(base + sp) * kDecodeRows + r];
-                const float a = fast_exp2(ml.x - M);
-                acc += a * part_o[((base + sp) * kDecodeRows + r) * D + c];
-                lsum += a * ml.y;
+        for (int s0 = lane; s0 < nsplit; s0 += 32) M = fmaxf(M, part_ml[(base + s0) * kDecodeRows + r].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float acc[kPer];
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+        float lsum = 0.f;
+        if (M != -INFINITY) {
+            for (int c0 = 0; c0 < nsplit; c0 += 32) {
+                float w = 0.f;
+                if (c0 + lane < nsplit) {
+                    const float2 ml = part_ml[(base + c0 + lane) * kDecodeRows + r];
+                    w = fast_exp2(ml.x - M);
+                    lsum += w * ml.y;
+                }
+                const int n = min(32, nsplit - c0);
+                const float* src0 = part_o + ((base + c0) * kDecodeRows + r) * D + lane * kPer;
+                const long stride = (long)kDecodeRows * D;  // floats between consecutive splits
+                int j = 0;
+                for (; j + 4 <= n; j += 4) {  // four splits' loads in flight at once
+                    float v[4][kPer];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int c = 0; c < kPer; ++c) v[u][c] = __ldg(src0 + (j + u) * stride + c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float wj = __shfl_sync(0xffffffffu, w, j + u);
+#pragma unroll
+                        for (int c = 0; c < kPer; ++c) acc[c] += wj * v[u][c];
+                    }
+                }
+                for (; j < n; ++j) {
+                    const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+                    for (int c = 0; c < kPer; ++c) acc[c] += wj * __ldg(src0 + j * stride + c);
+                }
             }
-        const float val = lsum > 0.f ? acc / lsum : 0.f;
-        __nv_bfloat16 b = __float2bfloat16_rn(val);
-        out[((long)(q0 + r / g) * Hq + hk * g + r % g) * D + c] = *reinterpret_cast<uint16_t*>(&b);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        uint16_t* dst = out + ((long)(q0 + r / g) * Hq + hk * g + r % g) * D + lane * kPer;
+        if constexpr (kPer == 4)
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                        pack_bf16x2(acc[2] * inv, acc[3] * inv));
+        else
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
 }
 
@@ -507,10 +568,19 @@ static fa_status launch_decode(const void* q, const void* k_cache, const void* v
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     ++*launches;
     if (w.max_splits > 1) {
-        paged_merge_kernel<D><<<dim3(num_seqs, Hkv), 128, 0, s>>>(ctx_lens, q_lens, part_o, part_ml,
-                                                                  static_cast<uint16_t*>(out), Hq, Hkv,
-                                                                  w.split_blocks, w.max_splits, mbps);
-        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(num_seqs, Hkv);
+        cfg.blockDim = dim3(kMergeThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, paged_merge_kernel<D>, ctx_lens, q_lens, static_cast<const float*>(part_o),
+                               static_cast<const float2*>(part_ml), static_cast<uint16_t*>(out), Hq, Hkv,
+                               w.split_blocks, w.max_splits, mbps) != cudaSuccess)
+            return FA_ERR_CUDA;
         ++*launches;
     }
     return FA_OK;
