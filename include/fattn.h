@@ -69,7 +69,7 @@ const char* fa_status_string(fa_status status);
  * the causal mask when `causal` != 0; tile-by-tile processing).
  *   q   bf16 [B, T, Hq, d] row-major, 16-byte aligned
  *   k,v bf16 [B, T, Hkv, d]
- *   out bf16 [B, T, Hq, d] (written; may not alias the inputs)
+ *   out bf16 [B, T, Hq, d], 32-byte aligned (written; may not alias the inputs)
  *   lse fp32 [B, Hq, T] natural-log log-sum-exp of each row's scores, or NULL
  *   scale multiplies Q K^T (1/sqrt(d) for the textbook form); must be finite
  *         and > 0 (FA_ERR_INVALID_ARG otherwise)
@@ -132,7 +132,7 @@ fa_status fa_cache_append(const void* k, const void* v, void* k_cache, void* v_c
  *                chunk included (its queries sit at ctx - q_len .. ctx - 1)
  *   q_lens       int32 [num_seqs], 0 <= q_lens[s] <= ctx_lens[s];
  *                sum(q_lens) must equal total_q
- *   out          bf16 [total_q, Hq, d]
+ *   out          bf16 [total_q, Hq, d], 32-byte aligned
  *   max_q_len    host-side upper bound on every q_lens[s] (total_q is always
  *                a valid bound); used only to skip launching a kernel that
  *                would find no work

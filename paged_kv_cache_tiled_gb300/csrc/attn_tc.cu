@@ -55,7 +55,7 @@ struct TcCfg {
     static constexpr int kAtoms = D / 64;                 // 128-byte column blocks per row
     static constexpr int kAtomBytes = kTcRows * 128;      // one 128-row x 64-channel box
     static constexpr int kTileBytes = kAtoms * kAtomBytes;
-    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kStages = D == 128 ? 5 : 8;
     static constexpr int kQBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kStages * kTileBytes;
     static constexpr int kNumBars = 2 * kStages + 2 * 6 + 2;
@@ -100,6 +100,10 @@ struct Unit {
     int kt0;        // first KV tile to scan
     int n_kt;       // KV tiles to scan: [kt0, n_kt)
 };
+
+// Per-slot field of a unit.  A select instead of a runtime array index keeps
+// the value in a register (a runtime index would move the array to local memory).
+__device__ __forceinline__ int sel(const int (&a)[2], int s) { return s ? a[1] : a[0]; }
 
 // i-th unit of this CTA: units are ordered longest first and dealt to the CTAs
 // in boustrophedon order (round i goes left to right when even, right to left
@@ -203,11 +207,11 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
 template <int MODE>
 __device__ __forceinline__ int tile_class(const TcParams& p, const Unit& U, int s, int kt) {
     if constexpr (MODE == MODE_MASKED) {
-        if (U.nrows[s] <= 0) return 0;
+        if (sel(U.nrows, s) <= 0) return 0;
         const int nkt = (p.T + kTcRows - 1) / kTcRows;
-        return __ldg(p.cls + (long)(U.row0[s] / kTcRows) * nkt + kt);
+        return __ldg(p.cls + (long)(sel(U.row0, s) / kTcRows) * nkt + kt);
     } else {
-        return U.nrows[s] > 0 ? 1 : 0;
+        return sel(U.nrows, s) > 0 ? 1 : 0;
     }
 }
 
@@ -229,18 +233,16 @@ __device__ __forceinline__ bool unit_active(const TcParams& p, const Unit& U) {
 template <int D, int MODE>
 __device__ __forceinline__ uint16_t* out_row(const TcParams& p, const Unit& U, int s, int r) {
     if constexpr (MODE == MODE_PAGED)
-        return p.out + ((long)U.qtok[s] + r) * p.Hq * D + (long)U.head[s] * D;
+        return p.out + ((long)sel(U.qtok, s) + r) * p.Hq * D + (long)sel(U.head, s) * D;
     else
-        return p.out + (((long)U.b * p.T + U.row0[s] + r) * p.Hq + U.head[s]) * D;
+        return p.out + (((long)U.b * p.T + sel(U.row0, s) + r) * p.Hq + sel(U.head, s)) * D;
 }
 
-// A row that sees no key: output 0, LSE -inf.
-template <int D, int MODE>
-__device__ __noinline__ void store_zero_row(const TcParams& p, const Unit& U, int s, int r) {
-    uint16_t* orow = out_row<D, MODE>(p, U, s, r);
+// A row that sees no key: output 0, LSE -inf (lse may be null).
+template <int D>
+__device__ __noinline__ void store_zero_row(uint16_t* orow, float* lse) {
     for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-    if constexpr (MODE != MODE_PAGED)
-        if (p.lse) p.lse[((long)U.b * p.Hq + U.head[s]) * p.T + U.row0[s] + r] = -INFINITY;
+    if (lse) *lse = -INFINITY;
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -333,10 +335,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int a = 0; a < C::kAtoms; ++a) {
                         if constexpr (MODE == MODE_PAGED)
                             tma_load_4d(qbuf + s * C::kTileBytes + a * C::kAtomBytes, &tm_q, &qfull[s], a * 64,
-                                        U.head[s], U.qtok[s], 0);
+                                        sel(U.head, s), sel(U.qtok, s), 0);
                         else
                             tma_load_4d(qbuf + s * C::kTileBytes + a * C::kAtomBytes, &tm_q, &qfull[s], a * 64,
-                                        U.head[s], U.qtok[s], U.b);
+                                        sel(U.head, s), sel(U.qtok, s), U.b);
                     }
                 }
             }
@@ -397,19 +399,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
         constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
         const uint32_t q_addr = smem_u32(qbuf), ring_addr = smem_u32(ring);
-        const uint32_t s_col[2] = {C::kS0, C::kS1}, o_col[2] = {C::kO0, C::kO1};
-        int cons = 0, ucnt = 0, pc[2] = {0, 0};
+        auto s_col = [](int s) -> uint32_t { return s ? C::kS1 : C::kS0; };
+        auto o_col = [](int s) -> uint32_t { return s ? C::kO1 : C::kO0; };
+        int cons = 0, ucnt = 0, pc0 = 0, pc1 = 0;  // pc: P tiles consumed per slot
         bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
 
-        auto wait_v = [&](int vidx, int vkt, const Unit& U) -> bool {
+        auto wait_v = [&](int vidx, int vkt, int kv_len) -> bool {
             if (!mbar_wait_warp(&full[vidx % S], (vidx / S) & 1, lim_ns, abort_flag)) return false;
             if constexpr (MODE == MODE_PAGED) {
                 // Rows past the context inside the last partly filled block
                 // may hold stale words; zero them so a zero probability never
                 // meets a non-finite value.
                 const int kv0 = vkt * kTcRows;
-                const int z0 = U.kv_len - kv0;
-                const int z1 = min(kTcRows, ((U.kv_len + 15) & ~15) - kv0);
+                const int z0 = kv_len - kv0;
+                const int z1 = min(kTcRows, ((kv_len + 15) & ~15) - kv0);
                 if (z0 < z1) {
                     uint8_t* base = ring + (vidx % S) * C::kTileBytes;
                     const int n16 = (z1 - z0) * C::kAtoms * 8;
@@ -425,35 +428,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return true;
         };
+        // The start-address field of a descriptor is (address >> 4) in 14 bits;
+        // shared addresses stay below 256 KB, so advancing a descriptor by a byte
+        // offset is adding offset >> 4.
         auto issue_qk = [&](int s, int kidx) {
-            const uint32_t kb = ring_addr + (kidx % S) * C::kTileBytes;
-            const uint32_t qb = q_addr + s * C::kTileBytes;
+            const uint64_t kd = smem_desc_sw128(ring_addr + (kidx % S) * C::kTileBytes, 16, 1024);
+            const uint64_t qd = smem_desc_sw128(q_addr + s * C::kTileBytes, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
-                umma_ss(tbase + s_col[s], smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                        kIdescQK, kk > 0);
+                const uint32_t off = ((kk >> 2) * C::kAtomBytes + (kk & 3) * 32) >> 4;
+                umma_ss(tbase + s_col(s), qd + off, kd + off, kIdescQK, kk > 0);
             }
         };
         // O_s += P_s V over keys [64h, 64h+64) of the tile
         auto issue_pv_half = [&](int s, int vidx, int h, bool acc_first) {
-            const uint32_t vb = ring_addr + (vidx % S) * C::kTileBytes;
+            const uint64_t vd = smem_desc_sw128(ring_addr + (vidx % S) * C::kTileBytes, C::kAtomBytes, 1024);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const int kk = 4 * h + k4;
-                umma_ts(tbase + o_col[s], tbase + s_col[s] + kk * 8,
-                        smem_desc_sw128(vb + kk * 2048, C::kAtomBytes, 1024), kIdescPV, (acc_first || kk > 0));
+                umma_ts(tbase + o_col(s), tbase + s_col(s) + kk * 8, vd + (uint32_t)(kk * 2048 >> 4), kIdescPV,
+                        (acc_first || kk > 0));
             }
         };
         // waits for each half of P_s in turn and issues its P*V MMAs
         auto pv = [&](int s, int vidx, bool acc_first) -> bool {
             for (int h = 0; h < 2; ++h) {
-                if (!mbar_wait_warp(&pfull[2 * s + h], pc[s] & 1, lim_ns, abort_flag)) return false;
+                if (!mbar_wait_warp(&pfull[2 * s + h], (s ? pc1 : pc0) & 1, lim_ns, abort_flag)) return false;
                 tc_fence_after();
                 if (lane == 0) issue_pv_half(s, vidx, h, acc_first);
                 __syncwarp();
             }
-            ++pc[s];
+            if (s) ++pc1;
+            else ++pc0;
             return true;
         };
 
@@ -478,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after();
                 for (int s = 0; s < 2 && ok; ++s) {
                     if (it > 0) {
-                        if (s == 0 && !wait_v(prev_v, prev_kt, U)) {
+                        if (s == 0 && !wait_v(prev_v, prev_kt, U.kv_len)) {
                             ok = false;
                             break;
                         }
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 umma_commit(&qempty[0]);
                 umma_commit(&qempty[1]);
             }
-            if (!wait_v(prev_v, prev_kt, U)) {
+            if (!wait_v(prev_v, prev_kt, U.kv_len)) {
                 ok = false;
                 break;
             }
@@ -545,10 +551,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int u = unit_of(i, G);
             if (u >= num_units) continue;
             const Unit U = decode_unit<MODE>(p, u);
-            const bool valid = r < U.nrows[s];
-            const int row = U.row0[s] + r;  // row within T (dense) or within the chunk (paged)
+            const bool valid = r < sel(U.nrows, s);
+            const int row = sel(U.row0, s) + r;  // row within T (dense) or within the chunk (paged)
             if (!unit_active<MODE>(p, U)) {
-                if (valid) store_zero_row<D, MODE>(p, U, s, r);
+                if (valid) {
+                    float* lse = nullptr;
+                    if constexpr (MODE != MODE_PAGED)
+                        if (p.lse) lse = p.lse + ((long)U.b * p.Hq + sel(U.head, s)) * p.T + row;
+                    store_zero_row<D>(out_row<D, MODE>(p, U, s, r), lse);
+                }
                 continue;
             }
             // key j is visible when j <= row + pos_off (causal) and j < kv_len
@@ -574,7 +585,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // pass 1: row max, 64 columns per TMEM wait.  In the general case
                 // the masked, scaled logits are written back over S so that pass
                 // 2 reads them instead of re-reading the mask.
-                float mx = -INFINITY;
+                // 8 independent partial maxima / sums keep the reductions off a
+                // single serial dependency chain
+                float mxp[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
                 const bool vec_mask = mrow && ((p.T & 3) == 0);
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
@@ -584,7 +599,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_wait_ld();
                     if (plain) {  // scale > 0: the max of the raw scores gives the max of the scaled ones
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, __uint_as_float(raw[j]));
+                        for (int j = 0; j < 64; ++j) mxp[j & 7] = fmaxf(mxp[j & 7], __uint_as_float(raw[j]));
                     } else {
 #pragma unroll
                         for (int j4 = 0; j4 < 16; ++j4) {
@@ -604,13 +619,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                     ? -INFINITY
                                                     : fmaf(__uint_as_float(raw[4 * j4 + e]), p.scale_log2, mv[e] * kLog2e);
                                 raw[4 * j4 + e] = __float_as_uint(x);
-                                mx = fmaxf(mx, x);
+                                mxp[(4 * j4 + e) & 7] = fmaxf(mxp[(4 * j4 + e) & 7], x);
                             }
                         }
                         tmem_st32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
                         tmem_st32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     }
                 }
+                float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
                 if (plain) mx *= p.scale_log2;
                 else tmem_wait_st();
                 const float m_new = fmaxf(m, mx);
@@ -629,7 +646,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // pass 2: P = 2^(logit - m) as bf16.  Half h reads S columns
                 // [64h, 64h+64) and writes P columns [32h, 32h+32), only over S
                 // columns already read.
-                float rs = 0.f;
+                float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     uint32_t raw[64];
@@ -643,7 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int j = 0; j < 32; ++j) {
                         const float p0 = fast_exp2(fmaf(__uint_as_float(raw[2 * j]), sc2, neg_m));
                         const float p1 = fast_exp2(fmaf(__uint_as_float(raw[2 * j + 1]), sc2, neg_m));
-                        rs += p0 + p1;
+                        rsp[j & 7] += p0 + p1;
                         pk[j] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(trow + s_col + h * 32, pk);
@@ -654,7 +671,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mbar_arrive(&pfull[2 * s]);
                     mbar_arrive(&pfull[2 * s + 1]);
                 }
-                l += rs;
+                l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
                 if (rescale_o) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
@@ -682,26 +699,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const Unit E = decode_unit<MODE>(p, u);  // re-derived here so its fields are not live across the tile loop
             uint16_t* orow = out_row<D, MODE>(p, E, s, r);
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            // 64 columns per TMEM wait; 32-byte stores of the bf16 row
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(trow + o_col + c * 32, raw);
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t raw[64];
+                tmem_ld32(trow + o_col + c * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+                tmem_ld32(trow + o_col + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                 tmem_wait_ld();
-                uint32_t pk[16];
+                uint32_t pk[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
+                for (int j = 0; j < 32; ++j)
                     pk[j] = pack_bf16x2(__uint_as_float(raw[2 * j]) * inv_l, __uint_as_float(raw[2 * j + 1]) * inv_l);
                 if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-                    dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        st_global_v8(orow + c * 64 + q4 * 16, pk[8 * q4], pk[8 * q4 + 1], pk[8 * q4 + 2],
+                                     pk[8 * q4 + 3], pk[8 * q4 + 4], pk[8 * q4 + 5], pk[8 * q4 + 6], pk[8 * q4 + 7]);
                 }
             }
             if constexpr (MODE != MODE_PAGED)
                 if (p.lse && valid)
-                    p.lse[((long)E.b * p.Hq + E.head[s]) * p.T + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                    p.lse[((long)E.b * p.Hq + sel(E.head, s)) * p.T + row] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
         }
         if (!ok && lane == 0) fail();
     }
@@ -782,7 +800,7 @@ static fa_status check_prefill_args(const void* q, const void* k, const void* v,
     if ((d != 64 && d != 128) || Hq % Hkv != 0) return FA_ERR_UNSUPPORTED;
     if (B == 0 || T == 0) return FA_OK;
     if (!q || !k || !v || !out) return FA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned32(out)) return FA_ERR_INVALID_ARG;
     return FA_OK;
 }
 

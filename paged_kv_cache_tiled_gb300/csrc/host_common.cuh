@@ -32,6 +32,7 @@ fa_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 inline fa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 

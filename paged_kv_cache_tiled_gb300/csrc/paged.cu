@@ -608,7 +608,7 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
     if (block_size != kBS || (d != 64 && d != 128) || Hq % Hkv != 0) return FA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return FA_OK;
     if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !q_lens || !out) return FA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned32(out)) return FA_ERR_INVALID_ARG;
     if (num_blocks == 0 || max_blocks_per_seq == 0) return FA_ERR_INVALID_ARG;
     const PagedWs w = paged_ws_layout(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q);
     if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return FA_ERR_WORKSPACE;

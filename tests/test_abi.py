@@ -53,6 +53,9 @@ def test_host_validation(fattn):
     # null pointers / misalignment
     assert lib.fa_prefill(None, dummy, dummy, dummy, 1, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_INVALID_ARG
     assert lib.fa_prefill(P(4097), dummy, dummy, dummy, 1, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_INVALID_ARG
+    # outputs must be 32-byte aligned; non-positive scale is rejected
+    assert lib.fa_prefill(dummy, dummy, dummy, P(4096 + 16), 1, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_prefill(dummy, dummy, dummy, dummy, 1, 16, 4, 2, 64, 1, 0.0, None, None) == fattn.FA_ERR_INVALID_ARG
     # paged: block size other than 16 is unsupported
     assert lib.fa_paged_attn(dummy, dummy, dummy, dummy, dummy, dummy, dummy, 2, 4, 8, 4, 2, 64, 32, 1, 0.1, 2, 1,
                              dummy, 1 << 20, None) == fattn.FA_ERR_UNSUPPORTED
