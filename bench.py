@@ -7,8 +7,8 @@ config 4 long masked prefill, config 5 chunked prefill over the paged cache.
 
 Timing: W warm-up steps, then exactly K timed steps; each step's kernel work
 is bracketed by CUDA events on the launching stream and the L2 cache is
-flushed (a 2x-L2-sized buffer is overwritten) before every step, outside the
-events.  Barrier + synchronize on both sides of the timed region; the max over
+flushed before every step, outside the events (a 2x-L2 buffer is overwritten,
+then a second one is read, leaving only clean lines).  Barrier + synchronize on both sides of the timed region; the max over
 ranks is taken.  `e2e` repeats the primary step through the same C-ABI with
 the inputs in pinned host memory: host->device copies of q/k/v, the call and
 the device->host copy of the output are all inside the timed region.
@@ -148,7 +148,19 @@ class Timer:
     """Per-step CUDA-event timing on the current stream with an L2 flush before each step."""
 
     def __init__(self, flush_bytes: int):
+        # L2 flush: overwrite one 2x-L2 buffer, then read a second one, so the L2
+        # holds only clean lines of neither operand when the step starts (a
+        # write alone would leave dirty lines whose write-back the timed step
+        # would pay for)
         self.flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda")
+        self.flush_rd = torch.ones(flush_bytes // 4, dtype=torch.float32, device="cuda")
+
+    def flush_l2(self, i: int):
+        # ~100+ us of GPU work: it also keeps the GPU busy while the host
+        # enqueues the step, so no host-side gap falls between the events
+        self.flush.fill_(float(i))
+        self.flush_rd.sum()
+        self.flush_rd.sum()
 
     def run(self, step, steps: int, warmup: int, ws: int, sampler: ClockSampler | None = None,
             min_warm_s: float = 0.0):
@@ -156,7 +168,7 @@ class Timer:
         t0 = time.time()
         i = 0
         while i < warmup or (time.time() - t0) < min_warm_s:
-            self.flush.fill_(float(i))
+            self.flush_l2(i)
             step()
             i += 1
         torch.cuda.synchronize()
@@ -169,7 +181,7 @@ class Timer:
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for i in range(steps):
-            self.flush.fill_(float(i))
+            self.flush_l2(i)
             starts[i].record()
             step()
             ends[i].record()
@@ -412,7 +424,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded N(0,1) bf16 inputs with the shapes of config 2 (no weights needed)",
             "config": {"workload": "config 2: causal prefill B=4 T=2048 Hq=12 Hkv=2 d=128 bf16, scale 1/sqrt(128)",
-                       "l2": "flushed before every timed step (2x L2 buffer overwrite, outside the events)",
+                       "l2": "flushed before every timed step, outside the events: a 2x-L2 buffer is overwritten, then a second 2x-L2 buffer is read (clean L2)",
                        "replicas": ws},
             "roofline": roof, "e2e": e2e, "gpu_launches": res["launches"], "clocks": res["clocks"]}
 

@@ -164,11 +164,12 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
  * or fragment that pool), or a plugin interface that hands over inputs and
  * outputs but no scratch space.  This entry point takes the same arguments as
  * fa_paged_attn minus the workspace and uses instead a fixed scratch array of
- * FA_NOALLOC_SCRATCH_BYTES (16 MiB) that the library keeps on every GPU that
+ * FA_NOALLOC_SCRATCH_BYTES (32 MiB) that the library keeps on every GPU that
  * loads it, until the process exits.  It calls no allocator.
  *   - Problems whose fa_paged_attn_workspace_size(...) exceeds
  *     FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE before any
- *     launch (the decode partials grow with num_seqs * Hkv * splits * d).
+ *     launch (the scheduling lists grow with num_seqs and total_q; decode
+ *     partials take a fixed ~21 MB).
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
@@ -180,7 +181,7 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
  * Everything else -- arguments, layouts, results, errors -- is as for
  * fa_paged_attn.
  */
-#define FA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 fa_status fa_paged_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, const int32_t* ctx_lens,
                                 const int32_t* q_lens, void* out, int num_seqs,

@@ -6,10 +6,12 @@
 //
 // Decode rows (the section "FlashAttention-Style Kernels" notes that decode
 // has one or a few queries and is dominated by reading the growing cache)
-// take a bandwidth-bound split-KV kernel:
-//   * one CTA per (sequence, kv head, split of `split_blocks` blocks); its four
-//     warps take every fourth block of the split;
-//   * each warp streams its blocks through a private 3-stage ring of shared
+// take a bandwidth-bound kernel that streams the cache in balanced ranges:
+//   * the (sequence, kv head) segments are laid end to end as one stream of
+//     16-token pages; each of the grid's warps (one CTA of eight warps per SM)
+//     takes an equal contiguous range of pages, so every SM moves the same
+//     number of bytes whatever the mix of context lengths;
+//   * each warp streams its pages through a private 3-stage ring of shared
 //     memory with TMA (one 2 KB box per 64 channels of K and of V, 128-byte
 //     swizzled so the fragment loads below are bank-conflict free); the
 //     physical block id is read from the block table just before the copy;
@@ -18,13 +20,13 @@
 //     m16n8k16 warp MMAs, so K and V are read from HBM exactly once;
 //   * the running row max / row sum are kept in fp32 (online softmax with
 //     base-2 exponentials, scale * log2(e) folded into the scores);
-//   * the four warps' states are merged in shared memory; a single split
-//     writes the final bf16 output, several splits write fp32 partials
-//     (unnormalised O, running max, running sum) merged by a second kernel
-//     with log-sum-exp weights.
+//   * a segment inside one warp's range is written as final bf16 output; a
+//     segment cut by a range boundary leaves fp32 partials (unnormalised O,
+//     running max, running sum) that a second kernel merges with log-sum-exp
+//     weights.
 // Longer chunks take the tensor-core kernel (attn_tc.cu) through a work list
 // built on the device by `paged_meta_kernel`.
-#include <cstdlib>
+#include <algorithm>
 #include <mutex>
 
 #include "host_common.cuh"
@@ -32,8 +34,6 @@
 namespace fa {
 
 constexpr int kBS = 16;            // tokens per block
-constexpr int kDecodeWarps = 4;    // warps per decode CTA
-constexpr int kDecodeStages = 3;   // ring depth per warp
 constexpr int kDecodeRows = 16;    // M of the warp MMA
 
 // Launched from attn_tc.cu.
@@ -46,29 +46,23 @@ fa_status launch_paged_prefill(const void* q, const void* k_cache, const void* v
 __host__ __device__ inline bool is_decode_row(int q_len, int g) { return q_len >= 1 && g * q_len <= kDecodeRows; }
 
 // ------------------------------------------------------------------ layout --
+constexpr int kStreamWarps = 8;      // page streams per decode CTA
+constexpr int kStreamStages = 3;     // TMA ring depth per stream
+constexpr int kMaxStreamCtas = 160;  // decode grid cap (one CTA per SM); sizes the partial slots
+constexpr int kMaxStreamWarps = kMaxStreamCtas * kStreamWarps;
+
 struct PagedWs {
     size_t q_start, work_count, work_list, part_o, part_ml, total;
-    int split_blocks, max_splits, max_entries;
+    int max_entries;
 };
 
-// Blocks per decode split (per CTA).  FA_DECODE_SPLIT_BLOCKS (8..256) overrides
-// the default for tuning; the workspace size query uses the same value.
-inline int decode_split_blocks(int mbps) {
-    (void)mbps;
-    static const int v = [] {
-        const char* e = getenv("FA_DECODE_SPLIT_BLOCKS");
-        const int x = e ? atoi(e) : 0;
-        return (x >= 8 && x <= 256) ? x : 64;
-    }();
-    return v;
-}
-
+// Workspace: scheduling lists of the tensor-core path, then two partial slots
+// per decode stream warp (16 rows of fp32 O, plus (max, sum) per row).
 inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, int total_q) {
     (void)Hq;
+    (void)Hkv;
+    (void)mbps;
     PagedWs w{};
-    w.split_blocks = decode_split_blocks(mbps);
-    w.max_splits = (mbps + w.split_blocks - 1) / w.split_blocks;
-    if (w.max_splits < 1) w.max_splits = 1;
     w.max_entries = total_q / 128 + num_seqs + 1;
     size_t off = 0;
     w.q_start = off;
@@ -78,9 +72,9 @@ inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, i
     w.work_list = off;
     off = align256(off + sizeof(int32_t) * 2 * (size_t)w.max_entries);
     w.part_o = off;
-    off = align256(off + sizeof(float) * (size_t)num_seqs * Hkv * w.max_splits * kDecodeRows * d);
+    off = align256(off + sizeof(float) * (size_t)2 * kMaxStreamWarps * kDecodeRows * d);
     w.part_ml = off;
-    off = align256(off + sizeof(float2) * (size_t)num_seqs * Hkv * w.max_splits * kDecodeRows);
+    off = align256(off + sizeof(float2) * (size_t)2 * kMaxStreamWarps * kDecodeRows);
     w.total = off;
     return w;
 }
@@ -102,65 +96,213 @@ __device__ int cta_prefix(const int32_t* __restrict__ q_lens, int s, int* red) {
 }
 
 // -------------------------------------------------------------- decode -----
+// Work is balanced by pages: the decode segments (sequence, kv head) are laid
+// end to end, sequence-major, as one stream of 16-token pages; warp w of the
+// grid takes pages [w*P/W, (w+1)*P/W).  A segment that lies inside one warp's
+// range is finished by that warp (bf16 output); a segment cut by a range
+// boundary leaves per-warp partials (running max, row sum, unnormalised O) in
+// slot 2w (the warp's first segment) or 2w+1 (its last), and the merge kernel
+// combines them.  Every page is read once; every warp streams the same number
+// of bytes, so no SM waits on a long sequence.
+
+// Pages one kv head of sequence s contributes to the decode stream (0 when the
+// sequence takes the tensor-core path or its lengths are inconsistent).
+__device__ __forceinline__ int decode_blocks(const int32_t* __restrict__ q_lens, const int32_t* __restrict__ ctx_lens,
+                                             int s, int g, int mbps) {
+    const int ql = __ldg(q_lens + s), cl = __ldg(ctx_lens + s);
+    if (!is_decode_row(ql, g) || ql > cl || cl > mbps * kBS) return 0;
+    return (cl + kBS - 1) / kBS;
+}
+
+// The stream partition: warp w of W starts at page floor(w * P / W).  With
+// P = qt * W + rm this is w * qt + (w * rm) / W, where (w * rm) < W * W fits
+// 32 bits: one 64-bit division per kernel instead of one per lookup.
+struct StreamSplit {
+    long long P, qt;
+    int rm, W;
+    __device__ StreamSplit(long long P_, int W_) : P(P_), qt(P_ / W_), rm((int)(P_ - P_ / W_ * W_)), W(W_) {}
+    __device__ __forceinline__ long long begin(int w) const {
+        return (long long)w * qt + (int)((unsigned)w * (unsigned)rm / (unsigned)W);
+    }
+    // warp whose range holds page x (0 <= x < P)
+    __device__ __forceinline__ int owner(long long x) const {
+        int w = (int)min((long long)W - 1, x * W / P);  // within one of the owner
+        while (w + 1 < W && begin(w + 1) <= x) ++w;
+        while (w > 0 && begin(w) > x) --w;
+        return w;
+    }
+};
+
+// Sum over the CTA (blockDim.x a multiple of 32, at most 32 warps).
+__device__ long long cta_sum_ll(long long v, long long* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    long long t = 0;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    __syncthreads();
+    return t;
+}
+
 template <int D>
-struct DecodeSmem {
-    static constexpr int kPage = kBS * D * 2;                      // bytes of one K (or V) page
-    static constexpr int kStage = 2 * kPage;                       // K page + V page
-    static constexpr int kRing = kDecodeWarps * kDecodeStages * kStage;
-    static constexpr int kCombine = kDecodeWarps * kDecodeRows * (D + 2) * 4;
-    static constexpr int kData = kRing > kCombine ? kRing : kCombine;
-    static constexpr int kBytes = 1024 /*align slack*/ + kData + (kDecodeWarps * kDecodeStages + 1) * 8 + 64;
+struct StreamSmem {
+    static constexpr int kPage = kBS * D * 2;  // bytes of one K (or V) page
+    static constexpr int kStage = 2 * kPage;   // K page + V page
+    static constexpr int kRing = kStreamWarps * kStreamStages * kStage;
+    static constexpr int kBars = kStreamWarps * kStreamStages + 1;
+    static constexpr int kBytes = 1024 /*align slack*/ + kRing + kBars * 8 + 512;
+};
+
+// Position of a stream cursor: sequence, kv head, block within the sequence.
+struct Cursor {
+    int s, hk, blk, nblk;  // nblk: pages per kv head of sequence s
+    int q0;                // first packed query row of sequence s
 };
 
 template <int D>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 2)
+__global__ void __launch_bounds__(kStreamWarps * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const uint16_t* __restrict__ q, const int32_t* __restrict__ bt,
                         const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ q_lens,
                         uint16_t* __restrict__ out, float* __restrict__ part_o, float2* __restrict__ part_ml,
-                        int mbps, int num_blocks, int Hq, int Hkv, int causal, float scale_log2, int split_blocks,
-                        int max_splits, DevCtx ctx) {
-    using L = DecodeSmem<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kData);
-    uint64_t* never = bars + kDecodeWarps * kDecodeStages;  // nothing arrives on it (time-out test hook)
-    int* red = reinterpret_cast<int*>(never + 1);
-    volatile int* abort_flag = red + 8;
-
+                        int num_seqs, int mbps, int num_blocks, int Hq, int Hkv, int causal, float scale_log2,
+                        DevCtx ctx) {
     // the merge kernel that follows may be scheduled now; it waits for this
     // grid's completion before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int sp = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
-    const int g = Hq / Hkv;
-    const int q_len = __ldg(q_lens + s), ctx_len = __ldg(ctx_lens + s);
-    if (!is_decode_row(q_len, g)) return;
-    if (q_len > ctx_len || ctx_len > mbps * kBS) {
-        if (sp == 0 && hk == 0 && threadIdx.x == 0) raise_error(ctx, ERR_BOUNDS_BIT);
-        return;
-    }
-    const int nblk = (ctx_len + kBS - 1) / kBS;
-    const int nsplit = (nblk + split_blocks - 1) / split_blocks;
-    if (sp >= nsplit) return;
-    const int blk0 = sp * split_blocks, blk1 = min(nblk, blk0 + split_blocks);
-    const int nrows = g * q_len;
+    using L = StreamSmem<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kRing);
+    uint64_t* never = bars + kStreamWarps * kStreamStages;  // nothing arrives on it (time-out test hook)
+    long long* red = reinterpret_cast<long long*>(never + 1);  // 2 * kStreamWarps entries
+    int* start_s = reinterpret_cast<int*>(red + 2 * kStreamWarps);  // per warp: first sequence, page offset, q0
+    int* start_off = start_s + kStreamWarps;
+    int* start_q0 = start_off + kStreamWarps;
+    volatile int* abort_flag = start_q0 + kStreamWarps;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = Hq / Hkv;
+    const int W = gridDim.x * kStreamWarps;
+    const int gw = blockIdx.x * kStreamWarps + warp;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kDecodeWarps * kDecodeStages + 1; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < L::kBars; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
+    if (threadIdx.x < kStreamWarps) start_s[threadIdx.x] = -1;
+
+    // pass 1: total pages P (and length checks).  With at most blockDim.x
+    // sequences each thread keeps its sequence's values for pass 2.
+    long long mine = 0;
+    const bool one_chunk = num_seqs <= (int)blockDim.x;
+    long long my_n = 0, my_q = 0;
+    if (one_chunk && threadIdx.x < num_seqs) {
+        my_n = (long long)Hkv * decode_blocks(q_lens, ctx_lens, threadIdx.x, g, mbps);
+        my_q = __ldg(q_lens + threadIdx.x);
+    }
+    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+        const int ql = __ldg(q_lens + s), cl = __ldg(ctx_lens + s);
+        if (!is_decode_row(ql, g)) continue;
+        if (ql > cl || cl > mbps * kBS) {
+            if (blockIdx.x == 0) raise_error(ctx, ERR_BOUNDS_BIT);
+            continue;
+        }
+        mine += (cl + kBS - 1) / kBS;
+    }
+    const long long P = (long long)Hkv * cta_sum_ll(mine, red);
+    // pass 2: locate the first page of this CTA's warps (prefix scan over sequences)
+    const StreamSplit split(P, W);
+    long long first[kStreamWarps];
+#pragma unroll
+    for (int i = 0; i < kStreamWarps; ++i) first[i] = split.begin(blockIdx.x * kStreamWarps + i);
+    const long long cta_end = split.begin((blockIdx.x + 1) * kStreamWarps);
+    long long carry_p = 0, carry_q = 0;
+    for (int base = 0; base < num_seqs && carry_p < cta_end; base += blockDim.x) {
+        const int s = base + threadIdx.x;
+        long long n = 0, ql = 0;
+        if (one_chunk) {
+            n = my_n;
+            ql = my_q;
+        } else if (s < num_seqs) {
+            n = (long long)Hkv * decode_blocks(q_lens, ctx_lens, s, g, mbps);
+            ql = __ldg(q_lens + s);
+        }
+        // inclusive scans of pages and query rows within this chunk
+        long long xp = n, xq = ql;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long yp = __shfl_up_sync(0xffffffffu, xp, o), yq = __shfl_up_sync(0xffffffffu, xq, o);
+            if (lane >= o) {
+                xp += yp;
+                xq += yq;
+            }
+        }
+        __syncthreads();
+        if (lane == 31) {
+            red[warp] = xp;
+            red[kStreamWarps + warp] = xq;
+        }
+        __syncthreads();
+        long long off_p = carry_p, off_q = carry_q, tot_p = 0, tot_q = 0;
+        for (int i = 0; i < kStreamWarps; ++i) {
+            if (i < warp) {
+                off_p += red[i];
+                off_q += red[kStreamWarps + i];
+            }
+            tot_p += red[i];
+            tot_q += red[kStreamWarps + i];
+        }
+        const long long excl_p = off_p + xp - n, excl_q = off_q + xq - ql;
+        if (n > 0)
+#pragma unroll
+            for (int i = 0; i < kStreamWarps; ++i)
+                if (first[i] >= excl_p && first[i] < excl_p + n) {
+                    start_s[i] = s;
+                    start_off[i] = (int)(first[i] - excl_p);
+                    start_q0[i] = (int)excl_q;
+                }
+        carry_p += tot_p;
+        carry_q += tot_q;
+    }
     __syncthreads();
 
-    uint8_t* ring = smem + warp * kDecodeStages * L::kStage;
-    uint64_t* wbar = bars + warp * kDecodeStages;
-    const int n_mine = (blk1 - blk0 - warp + kDecodeWarps - 1) / kDecodeWarps;  // blocks blk0+warp+4i
+    const long long b0 = split.begin(gw), b1 = split.begin(gw + 1);
+    const int n_pages = (int)(b1 - b0);
+    if (n_pages <= 0 || start_s[warp] < 0) return;  // no more CTA-wide synchronisation below
 
+    uint8_t* ring = smem + warp * kStreamStages * L::kStage;
+    uint64_t* wbar = bars + warp * kStreamStages;
+    // advances a cursor by one page; entering a new sequence skips the ones
+    // with no decode pages and carries the packed query offset along
+    auto advance = [&](Cursor& c) {
+        if (++c.blk < c.nblk) return;
+        c.blk = 0;
+        if (++c.hk < Hkv) return;
+        c.hk = 0;
+        do {
+            c.q0 += __ldg(q_lens + c.s);
+            ++c.s;
+            c.nblk = c.s < num_seqs ? decode_blocks(q_lens, ctx_lens, c.s, g, mbps) : 0;
+        } while (c.s < num_seqs && c.nblk == 0);
+    };
+    Cursor start;
+    start.s = start_s[warp];
+    start.nblk = decode_blocks(q_lens, ctx_lens, start.s, g, mbps);
+    start.hk = start_off[warp] / start.nblk;
+    start.blk = start_off[warp] % start.nblk;
+    start.q0 = start_q0[warp];
+
+    Cursor ci = start;  // issue cursor (lane 0 only)
+    // lane 0 reads the block-table entry of the next page one issue ahead, so
+    // that load's latency is not on the copy's path
+    int next_phys = lane == 0 ? __ldg(bt + (long)ci.s * mbps + ci.blk) : 0;
     auto issue = [&](int i) {
-        const int stage = i % kDecodeStages;
-        const int lb = blk0 + warp + kDecodeWarps * i;
-        int phys = __ldg(bt + (long)s * mbps + lb);
+        const int stage = i % kStreamStages;
+        int phys = next_phys;
         if (phys < 0 || phys >= num_blocks) {
             raise_error(ctx, ERR_BOUNDS_BIT);
             phys = num_blocks;  // outside the tensor map: the copy fills zeros
@@ -170,9 +312,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         mbar_arrive_expect_tx(&wbar[stage], L::kStage);
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-            tma_load_4d(kp + h * 2048, &tm_k, &wbar[stage], h * 64, 0, hk, phys);
-            tma_load_4d(vp + h * 2048, &tm_v, &wbar[stage], h * 64, 0, hk, phys);
+            tma_load_4d(kp + h * 2048, &tm_k, &wbar[stage], h * 64, 0, ci.hk, phys);
+            tma_load_4d(vp + h * 2048, &tm_v, &wbar[stage], h * 64, 0, ci.hk, phys);
         }
+        advance(ci);
+        if (i + 1 < n_pages) next_phys = __ldg(bt + (long)ci.s * mbps + ci.blk);
     };
     bool ok = !ctx.force_timeout || mbar_wait_warp(never, 0, ctx.wait_ns, abort_flag);
     if (!ok && lane == 0) {
@@ -181,21 +325,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     }
     int issued = 0;  // lane 0's count of copies issued
     if (lane == 0 && ok)
-        for (; issued < n_mine && issued < kDecodeStages; ++issued) issue(issued);
-    // the first copies are in flight; the query offset is computed meanwhile
-    const int q0 = cta_prefix(q_lens, s, red);
+        for (; issued < n_pages && issued < kStreamStages; ++issued) issue(issued);
 
-    // Q fragments (A operand, rows r = token * g + head-in-group)
-    const int gid = lane >> 2, tig = lane & 3;
+    const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, r8 = lane & 7;
+    Cursor cc = start;            // compute cursor (all lanes)
+    long long seg_first = b0 - start.blk;  // global index of the current segment's first page
+    int ctx_len = 0, q_len = 0, nrows = 0, pos_r0 = 0, pos_r1 = 0;
     uint32_t qa[D / 16][4];
-    {
-        const int rows_[2] = {gid, gid + 8};
+    float o[D / 8][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    // starts segment (cc.s, cc.hk): loads its query rows as MMA A fragments
+    // (rows r = token * g + head-in-group) and resets the softmax state
+    auto begin_segment = [&]() {
+        ctx_len = __ldg(ctx_lens + cc.s);
+        q_len = __ldg(q_lens + cc.s);
+        nrows = g * q_len;
+        const int rr[2] = {gid, gid + 8};
         const uint16_t* qrow[2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = rows_[i];
-            qrow[i] = r < nrows ? q + ((long)(q0 + r / g) * Hq + hk * g + r % g) * D : nullptr;
-        }
+        for (int i = 0; i < 2; ++i)
+            qrow[i] = rr[i] < nrows ? q + ((long)(cc.q0 + rr[i] / g) * Hq + cc.hk * g + rr[i] % g) * D : nullptr;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const int c = ks * 16 + tig * 2;
@@ -204,21 +354,60 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             qa[ks][2] = qrow[0] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[0] + c + 8)) : 0u;
             qa[ks][3] = qrow[1] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[1] + c + 8)) : 0u;
         }
-    }
-    // causal limit per fragment row: keys <= pos(row) are visible
-    const int pos_r0 = causal ? ctx_len - q_len + gid / g : ctx_len - 1;
-    const int pos_r1 = causal ? ctx_len - q_len + (gid + 8) / g : ctx_len - 1;
-
-    float o[D / 8][4];
+        // keys <= pos(row) are visible
+        pos_r0 = causal ? ctx_len - q_len + gid / g : ctx_len - 1;
+        pos_r1 = causal ? ctx_len - q_len + (gid + 8) / g : ctx_len - 1;
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    };
+    // finishes the current segment: final bf16 rows when the whole segment
+    // was in this warp's range, otherwise a partial in slot 2*gw + side
+    auto end_segment = [&]() {
+        float la = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+        la += __shfl_xor_sync(0xffffffffu, la, 2);
+        float lb = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+        lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+        const bool whole = seg_first >= b0 && seg_first + cc.nblk <= b1;
+        const int rr[2] = {gid, gid + 8};
+        const float ml[2] = {m0, m1}, ls[2] = {la, lb};
+        if (whole) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int r = rr[i];
+                if (r >= nrows) continue;
+                const float inv = ls[i] > 0.f ? 1.f / ls[i] : 0.f;
+                uint16_t* dst = out + ((long)(cc.q0 + r / g) * Hq + cc.hk * g + r % g) * D;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n)
+                    *reinterpret_cast<uint32_t*>(dst + n * 8 + tig * 2) =
+                        pack_bf16x2(o[n][2 * i] * inv, o[n][2 * i + 1] * inv);
+            }
+        } else {
+            const long slot = 2L * gw + (seg_first <= b0 ? 0 : 1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int r = rr[i];
+                if (r >= nrows) continue;
+                float* dst = part_o + (slot * kDecodeRows + r) * D;
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n)
+                    *reinterpret_cast<float2*>(dst + n * 8 + tig * 2) = make_float2(o[n][2 * i], o[n][2 * i + 1]);
+                if (tig == 0) part_ml[slot * kDecodeRows + r] = make_float2(ml[i], ls[i]);
+            }
+        }
+    };
 
-    const int mi = lane >> 3, r8 = lane & 7;
     int consumed = 0;
-    for (int i = 0; ok && i < n_mine; ++i, consumed = i) {
-        const int stage = i % kDecodeStages;
-        if (!mbar_wait_warp(&wbar[stage], (i / kDecodeStages) & 1, ctx.wait_ns, abort_flag)) {
+    if (ok) begin_segment();
+    for (int i = 0; ok && i < n_pages; ++i, consumed = i) {
+        if (i > 0 && cc.blk == 0) {  // the cursor entered a new segment
+            seg_first = b0 + i;
+            begin_segment();
+        }
+        const int stage = i % kStreamStages;
+        if (!mbar_wait_warp(&wbar[stage], (i / kStreamStages) & 1, ctx.wait_ns, abort_flag)) {
             if (lane == 0) {
                 raise_error(ctx, ERR_TIMEOUT_BIT);
                 *abort_flag = 1;
@@ -228,8 +417,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         }
         const uint32_t kbase = smem_u32(ring + stage * L::kStage);
         const uint32_t vbase = kbase + L::kPage;
-        const int lb = blk0 + warp + kDecodeWarps * i;
-        const int tok0 = lb * kBS;
+        const int tok0 = cc.blk * kBS;
 
         // S = Q K^T : 16 rows x 16 tokens
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -237,10 +425,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         for (int ks = 0; ks < D / 16; ++ks) {
             const int tok = (mi >> 1) * 8 + r8;
             const int chunk = ks * 2 + (mi & 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0, b1, b2, b3);
-            mma_bf16_16816(sc[0], qa[ks], b0, b1);
-            mma_bf16_16816(sc[1], qa[ks], b2, b3);
+            uint32_t b0r, b1r, b2r, b3r;
+            ldsm_x4(kbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0r, b1r, b2r, b3r);
+            mma_bf16_16816(sc[0], qa[ks], b0r, b1r);
+            mma_bf16_16816(sc[1], qa[ks], b2r, b3r);
         }
         // mask + online softmax (base 2)
         float x[2][4];
@@ -263,16 +451,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         const float a0 = fast_exp2(m0 - mu0), a1 = fast_exp2(m1 - mu1);
         m0 = mn0;
         m1 = mn1;
-        float p[2][4];
+        float pr[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            p[nt][0] = fast_exp2(x[nt][0] - mu0);
-            p[nt][1] = fast_exp2(x[nt][1] - mu0);
-            p[nt][2] = fast_exp2(x[nt][2] - mu1);
-            p[nt][3] = fast_exp2(x[nt][3] - mu1);
+            pr[nt][0] = fast_exp2(x[nt][0] - mu0);
+            pr[nt][1] = fast_exp2(x[nt][1] - mu0);
+            pr[nt][2] = fast_exp2(x[nt][2] - mu1);
+            pr[nt][3] = fast_exp2(x[nt][3] - mu1);
         }
-        l0 = l0 * a0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-        l1 = l1 * a1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+        l0 = l0 * a0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
+        l1 = l1 * a1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
         if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
             for (int n = 0; n < D / 8; ++n) {
@@ -282,170 +470,166 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
                 o[n][3] *= a1;
             }
         }
-        uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(p[0][2], p[0][3]),
-                          pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(p[1][2], p[1][3])};
+        uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
+                          pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
         // O += P V : V rows past the context are zeroed so stale cache words
         // (possibly NaN) cannot reach the accumulator through a zero weight
         const int nvalid = ctx_len - tok0;  // >= 1
-        const uint32_t zlo0 = (tig * 2 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t zhi0 =
-            (tig * 2 + 8 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 9 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t zlo = (tig * 2 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t zhi = (tig * 2 + 8 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 9 < nvalid ? 0xffff0000u : 0u);
 #pragma unroll
         for (int dn = 0; dn < D / 16; ++dn) {
             const int tok = (mi & 1) * 8 + r8;
             const int chunk = dn * 2 + (mi >> 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0, b1, b2, b3);
-            b0 &= zlo0;
-            b2 &= zlo0;
-            b1 &= zhi0;
-            b3 &= zhi0;
-            mma_bf16_16816(o[2 * dn], pa, b0, b1);
-            mma_bf16_16816(o[2 * dn + 1], pa, b2, b3);
+            uint32_t b0r, b1r, b2r, b3r;
+            ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0r, b1r, b2r, b3r);
+            b0r &= zlo;
+            b2r &= zlo;
+            b1r &= zhi;
+            b3r &= zhi;
+            mma_bf16_16816(o[2 * dn], pa, b0r, b1r);
+            mma_bf16_16816(o[2 * dn + 1], pa, b2r, b3r);
         }
         __syncwarp();
-        if (lane == 0 && issued < n_mine) issue(issued++);
+        if (lane == 0 && issued < n_pages) issue(issued++);
+        // leaving the segment: last page of the range or of the segment
+        const bool last_here = (i + 1 == n_pages) || (cc.blk + 1 == cc.nblk);
+        if (last_here) end_segment();
+        advance(cc);
     }
     if (!ok && lane == 0) {
         // drain: let the copies this warp issued but did not consume land
         // before the CTA can exit
         for (int i = consumed; i < issued; ++i)
-            (void)mbar_wait_bounded(&wbar[i % kDecodeStages], (i / kDecodeStages) & 1, 1000000000ull, nullptr);
-    }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-    __syncthreads();  // ring no longer read; reuse it for the cross-warp merge
-    if (*abort_flag) return;
-    float* ow = reinterpret_cast<float*>(smem);                       // [warp][row][D]
-    float* mlw = ow + kDecodeWarps * kDecodeRows * D;                  // [warp][row][2]
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-        const int c = n * 8 + tig * 2;
-        ow[(warp * kDecodeRows + gid) * D + c] = o[n][0];
-        ow[(warp * kDecodeRows + gid) * D + c + 1] = o[n][1];
-        ow[(warp * kDecodeRows + gid + 8) * D + c] = o[n][2];
-        ow[(warp * kDecodeRows + gid + 8) * D + c + 1] = o[n][3];
-    }
-    if (tig == 0) {
-        mlw[(warp * kDecodeRows + gid) * 2] = m0;
-        mlw[(warp * kDecodeRows + gid) * 2 + 1] = l0;
-        mlw[(warp * kDecodeRows + gid + 8) * 2] = m1;
-        mlw[(warp * kDecodeRows + gid + 8) * 2 + 1] = l1;
-    }
-    __syncthreads();
-    const int per = blockDim.x / D > 0 ? blockDim.x / D : 1;  // threads per column group
-    const int c = threadIdx.x % D;
-    for (int r = threadIdx.x / D; r < nrows; r += per) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, mlw[(w * kDecodeRows + r) * 2]);
-        float acc = 0.f, lsum = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kDecodeWarps; ++w) {
-                const float a = fast_exp2(mlw[(w * kDecodeRows + r) * 2] - M);
-                acc += a * ow[(w * kDecodeRows + r) * D + c];
-                lsum += a * mlw[(w * kDecodeRows + r) * 2 + 1];
-            }
-        }
-        if (nsplit == 1) {
-            const float val = lsum > 0.f ? acc / lsum : 0.f;
-            __nv_bfloat16 b = __float2bfloat16_rn(val);
-            out[((long)(q0 + r / g) * Hq + hk * g + r % g) * D + c] = *reinterpret_cast<uint16_t*>(&b);
-        } else {
-            const long slot = (((long)s * Hkv + hk) * max_splits + sp) * kDecodeRows + r;
-            part_o[slot * D + c] = acc;
-            if (c == 0) part_ml[slot] = make_float2(M, lsum);
-        }
+            (void)mbar_wait_bounded(&wbar[i % kStreamStages], (i / kStreamStages) & 1, 1000000000ull, nullptr);
     }
 }
 
-// Merges split partials: m = max_s m_s, l = sum_s 2^(m_s - m) l_s,
-// O = sum_s 2^(m_s - m) O_s / l  (O_s unnormalised, all in base 2).
-// One warp per row (8 warps, rows strided), lane j owns channels 4j..4j+3 and
-// split j's statistics, so every load of a row is issued at once.  Launched as
-// a programmatic dependent of the decode kernel: it may start early and waits
-// for that grid's results with griddepcontrol.wait.
-constexpr int kMergeThreads = 256;
+// Merges the partials of segments cut by stream range boundaries: for row r,
+// m = max_p m_p, l = sum_p 2^(m_p - m) l_p, O = sum_p 2^(m_p - m) O_p / l (base
+// 2, O_p unnormalised).  One single-warp CTA per (sequence, kv head, row):
+// lane j owns channels 4j..4j+3 and piece j's statistics.  The CTAs are small
+// enough to be resident beside the decode kernel's, so the programmatic
+// launch lets them compute their offsets while it runs; they read partials
+// only after griddepcontrol.wait.
+constexpr int kMergeThreads = 32;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
                                                                     const int32_t* __restrict__ q_lens,
                                                                     const float* __restrict__ part_o,
                                                                     const float2* __restrict__ part_ml,
-                                                                    uint16_t* __restrict__ out, int Hq, int Hkv,
-                                                                    int split_blocks, int max_splits, int mbps) {
-    __shared__ int red[kMergeThreads / 32];
-    const int s = blockIdx.x, hk = blockIdx.y, g = Hq / Hkv;
-    const int q_len = __ldg(q_lens + s), ctx_len = __ldg(ctx_lens + s);
-    const bool active = is_decode_row(q_len, g) && q_len <= ctx_len && ctx_len <= mbps * kBS;
-    const int nblk = (ctx_len + kBS - 1) / kBS;
-    const int nsplit = (nblk + split_blocks - 1) / split_blocks;
-    if (!active || nsplit <= 1) {
-        // even a CTA with nothing to do waits for the decode grid, so this grid
-        // never completes ahead of the one it depends on
+                                                                    uint16_t* __restrict__ out, int num_seqs,
+                                                                    int Hq, int Hkv, int mbps, int W) {
+    const int s = blockIdx.x, hk = blockIdx.y, r = blockIdx.z, g = Hq / Hkv;
+    const int lane = threadIdx.x;
+    const int ql_s = __ldg(q_lens + s), cl_s = __ldg(ctx_lens + s);
+    const bool mine = is_decode_row(ql_s, g) && ql_s <= cl_s && cl_s <= mbps * kBS && r < g * ql_s;
+    if (!mine) {
+        // every CTA waits for the decode grid, so this grid never completes ahead of it
         asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
-    const int q0 = cta_prefix(q_lens, s, red);  // inputs only: no need to wait for the decode grid yet
+    const int nblk = (cl_s + kBS - 1) / kBS;
+    // inputs only so far: total pages, this sequence's first page and query row
+    long long tot = 0, pre = 0, q0 = 0;
+    for (int i = lane; i < num_seqs; i += 32) {
+        const int ql = __ldg(q_lens + i), cl = __ldg(ctx_lens + i);
+        const long long n = (is_decode_row(ql, g) && ql <= cl && cl <= mbps * kBS) ? (cl + kBS - 1) / kBS : 0;
+        tot += n;
+        if (i < s) {
+            pre += n;
+            q0 += ql;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        pre += __shfl_xor_sync(0xffffffffu, pre, o);
+        q0 += __shfl_xor_sync(0xffffffffu, q0, o);
+    }
+    const long long P = (long long)Hkv * tot;
+    const long long seg_first = (long long)Hkv * pre + (long long)hk * nblk;
+    const StreamSplit split(P, W);
+    const int w_lo = split.owner(seg_first), w_hi = split.owner(seg_first + nblk - 1);
+    const int npieces = w_hi - w_lo + 1;
+    // slot of piece k: 2w, or 2w+1 when the segment starts after warp w's first
+    // page; -1 when warp w's range is empty (fewer pages than warps: it wrote nothing)
+    auto slot_of = [&](int k) -> long {
+        const int w = w_lo + k;
+        const long long wb = split.begin(w);
+        if (split.begin(w + 1) == wb) return -1;
+        return 2L * w + (seg_first <= wb ? 0 : 1);
+    };
+    const long lane_slot = lane < npieces ? slot_of(lane) : -1;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int nrows = g * q_len;
-    const long base = ((long)s * Hkv + hk) * max_splits;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (w_lo == w_hi) return;  // the whole segment was finished by one warp of the decode kernel
+
     constexpr int kPer = D / 32;  // channels per lane
-    for (int r = warp; r < nrows; r += kMergeThreads / 32) {
-        float M = -INFINITY;
-        for (int s0 = lane; s0 < nsplit; s0 += 32) M = fmaxf(M, part_ml[(base + s0) * kDecodeRows + r].x);
+    float acc[kPer];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float acc[kPer];
+    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+    float lsum = 0.f, M = -INFINITY;
+    // pieces in groups of 32: lane j holds piece j's (max, sum); the running
+    // max of earlier groups rescales the accumulators
+    for (int c0 = 0; c0 < npieces; c0 += 32) {
+        const long myslot = c0 + lane < npieces ? (c0 == 0 ? lane_slot : slot_of(c0 + lane)) : -1;
+        const float2 ml = myslot >= 0 ? part_ml[myslot * kDecodeRows + r] : make_float2(-INFINITY, 0.f);
+        float gm = ml.x;
 #pragma unroll
-        for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
-        float lsum = 0.f;
-        if (M != -INFINITY) {
-            for (int c0 = 0; c0 < nsplit; c0 += 32) {
-                float w = 0.f;
-                if (c0 + lane < nsplit) {
-                    const float2 ml = part_ml[(base + c0 + lane) * kDecodeRows + r];
-                    w = fast_exp2(ml.x - M);
-                    lsum += w * ml.y;
+        for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+        const float Mn = fmaxf(M, gm);
+        if (Mn == -INFINITY) continue;  // nothing visible yet (uniform)
+        const float rescale = M == -INFINITY ? 0.f : fast_exp2(M - Mn);
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) acc[c] *= rescale;
+        lsum *= rescale;
+        M = Mn;
+        const float w = myslot >= 0 ? fast_exp2(ml.x - M) : 0.f;
+        lsum += w * ml.y;
+        const int n = min(32, npieces - c0);
+        int j = 0;
+        for (; j + 8 <= n; j += 8) {  // eight pieces' loads in flight at once
+            float v[8][kPer];
+            float wj[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                wj[u] = __shfl_sync(0xffffffffu, w, j + u);
+                const long sj = __shfl_sync(0xffffffffu, myslot, j + u);
+                const float* src = part_o + ((sj < 0 ? 0 : sj) * kDecodeRows + r) * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+                    v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+                } else {
+                    const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+                    v[u][0] = t.x; v[u][1] = t.y;
                 }
-                const int n = min(32, nsplit - c0);
-                const float* src0 = part_o + ((base + c0) * kDecodeRows + r) * D + lane * kPer;
-                const long stride = (long)kDecodeRows * D;  // floats between consecutive splits
-                int j = 0;
-                for (; j + 4 <= n; j += 4) {  // four splits' loads in flight at once
-                    float v[4][kPer];
+                if (sj < 0)  // an empty range wrote no partial: ignore whatever the slot holds
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-#pragma unroll
-                        for (int c = 0; c < kPer; ++c) v[u][c] = __ldg(src0 + (j + u) * stride + c);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float wj = __shfl_sync(0xffffffffu, w, j + u);
-#pragma unroll
-                        for (int c = 0; c < kPer; ++c) acc[c] += wj * v[u][c];
-                    }
-                }
-                for (; j < n; ++j) {
-                    const float wj = __shfl_sync(0xffffffffu, w, j);
-#pragma unroll
-                    for (int c = 0; c < kPer; ++c) acc[c] += wj * __ldg(src0 + j * stride + c);
-                }
+                    for (int c = 0; c < kPer; ++c) v[u][c] = 0.f;
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+            for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int c = 0; c < kPer; ++c) acc[c] += wj[u] * v[u][c];
         }
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        uint16_t* dst = out + ((long)(q0 + r / g) * Hq + hk * g + r % g) * D + lane * kPer;
-        if constexpr (kPer == 4)
-            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                                                        pack_bf16x2(acc[2] * inv, acc[3] * inv));
-        else
-            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        for (; j < n; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            const long sj = __shfl_sync(0xffffffffu, myslot, j);
+            if (sj < 0) continue;  // uniform across the warp
+            const float* src = part_o + (sj * kDecodeRows + r) * D + lane * kPer;
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) acc[c] += wj * __ldg(src + c);
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    uint16_t* dst = out + ((long)(q0 + r / g) * Hq + hk * g + r % g) * D + lane * kPer;
+    if constexpr (kPer == 4)
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+    else
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
 }
 
 // ------------------------------------------------------------ metadata -----
@@ -550,7 +734,7 @@ static fa_status launch_decode(const void* q, const void* k_cache, const void* v
     fa_status st = encode_tmap_bf16_4d(&tk, k_cache, dims, strides, box);
     if (st != FA_OK) return st;
     if ((st = encode_tmap_bf16_4d(&tv, v_cache, dims, strides, box)) != FA_OK) return st;
-    using L = DecodeSmem<D>;
+    using L = StreamSmem<D>;
     static bool attr_done = false;  // benign race: setting the attribute twice is harmless
     if (!attr_done) {
         if (cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) !=
@@ -561,28 +745,26 @@ static fa_status launch_decode(const void* q, const void* k_cache, const void* v
     float* part_o = reinterpret_cast<float*>(ws + w.part_o);
     float2* part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
     const float scale_log2 = scale * 1.4426950408889634f;
-    dim3 grid(w.max_splits, Hkv, num_seqs);
-    paged_decode_kernel<D><<<grid, kDecodeWarps * 32, L::kBytes, s>>>(
-        tk, tv, static_cast<const uint16_t*>(q), bt, ctx_lens, q_lens, static_cast<uint16_t*>(out), part_o,
-        part_ml, mbps, num_blocks, Hq, Hkv, causal, scale_log2, w.split_blocks, w.max_splits, ctx);
+    const int grid = std::min(sm_count(), kMaxStreamCtas);
+    paged_decode_kernel<D><<<grid, kStreamWarps * 32, L::kBytes, s>>>(
+        tk, tv, static_cast<const uint16_t*>(q), bt, ctx_lens, q_lens, static_cast<uint16_t*>(out), part_o, part_ml,
+        num_seqs, mbps, num_blocks, Hq, Hkv, causal, scale_log2, ctx);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     ++*launches;
-    if (w.max_splits > 1) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(num_seqs, Hkv);
-        cfg.blockDim = dim3(kMergeThreads);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, paged_merge_kernel<D>, ctx_lens, q_lens, static_cast<const float*>(part_o),
-                               static_cast<const float2*>(part_ml), static_cast<uint16_t*>(out), Hq, Hkv,
-                               w.split_blocks, w.max_splits, mbps) != cudaSuccess)
-            return FA_ERR_CUDA;
-        ++*launches;
-    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_seqs, Hkv, kDecodeRows);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_merge_kernel<D>, ctx_lens, q_lens, static_cast<const float*>(part_o),
+                           static_cast<const float2*>(part_ml), static_cast<uint16_t*>(out), num_seqs, Hq, Hkv,
+                           mbps, grid * kStreamWarps) != cudaSuccess)
+        return FA_ERR_CUDA;
+    ++*launches;
     return FA_OK;
 }
 

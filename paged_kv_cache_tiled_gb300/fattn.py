@@ -26,7 +26,7 @@ EXPORTS = [
     "fa_cache_append", "fa_paged_attn_workspace_size", "fa_paged_attn", "fa_get_error", "fa_debug_gather_kv",
     "fa_debug_set_wait_limit", "fa_debug_force_timeout", "fa_last_launch_count", "fa_paged_attn_noalloc",
 ]
-NOALLOC_SCRATCH_BYTES = 16 << 20  # FA_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
 
 class FattnError(RuntimeError):
@@ -209,7 +209,7 @@ def fa_paged_attn(q, k_cache, v_cache, block_table, ctx_lens, q_lens, causal: bo
 def fa_paged_attn_noalloc(q, k_cache, v_cache, block_table, ctx_lens, q_lens, causal: bool = True,
                           scale: float | None = None, out=None, max_q_len: int | None = None, stream=None):
     """fa_paged_attn without a workspace, for callers that cannot allocate device
-    scratch: the library's fixed 16 MiB per-device array is used instead.  Calls
+    scratch: the library's fixed 32 MiB per-device array is used instead.  Calls
     must not overlap on the GPU (they share that array)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)

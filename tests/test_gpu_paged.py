@@ -160,3 +160,15 @@ def test_corrupt_block_table_is_reported(F):
     out, kc, vc, st = run_paged(F, p, append=False, out_guard=True)
     assert st == F.FA_ERR_BOUNDS
     assert torch.isfinite(out.float()).all()
+
+
+def test_decode_stream_range_boundaries(F):
+    """Decode work is split into equal page ranges per warp: many tiny segments
+    fall inside one range, and one long segment spans many ranges (its partials
+    are merged); every row still matches the oracle."""
+    ctx_old = [0, 1, 15, 16, 31, 12000, 2, 47, 63, 64, 300, 0, 9, 100, 4, 1]
+    p = W.paged_case(46, ctx_old, [1] * len(ctx_old), 12, 2, 128, num_blocks=1200)
+    out, kc, vc, st = run_paged(F, p, max_q_len=1, out_guard=True)
+    assert st == F.FA_OK
+    ref, _, _ = oracle_paged(p, bits(kc), bits(vc))
+    assert_parity(out, ref, "stream boundaries")
