@@ -48,17 +48,30 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_hash():
+    import hashlib
+    import glob
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_tiled_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic():
-    """Per-launch DRAM bytes from committed ncu summaries (lines 'traffic <kernel-key> <bytes>')."""
-    out = {}
+    """Per-launch DRAM bytes from committed ncu summaries (lines 'traffic <kernel-key> <bytes>'),
+    used only while the kernel sources are the ones the counters were taken on."""
+    out, src = {}, None
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if os.path.exists(path):
         with open(path) as f:
             for line in f:
                 parts = line.split()
+                if len(parts) == 2 and parts[0] == "source":
+                    src = parts[1]
                 if len(parts) == 3 and parts[0] == "traffic":
                     out[parts[1]] = float(parts[2])
-    return out
+    return out if src == kernel_source_hash() else {}
 
 
 # ------------------------------------------------------------ distributed ---
