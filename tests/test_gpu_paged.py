@@ -172,3 +172,28 @@ def test_decode_stream_range_boundaries(F):
     assert st == F.FA_OK
     ref, _, _ = oracle_paged(p, bits(kc), bits(vc))
     assert_parity(out, ref, "stream boundaries")
+
+
+def test_decode_workspace_needs_no_clearing(F):
+    """The decode path's workspace (partials of segments cut by range
+    boundaries, read back by the merge) needs no clearing: a workspace holding
+    any bytes (all ones, random words, a previous call's contents) gives the
+    same output as a zeroed one."""
+    p = W.paged_case(47, [3000, 17, 900, 4000, 260], [1, 1, 1, 1, 1], 12, 2, 128, num_blocks=700)
+    kc, vc = p.k_cache.cuda(), p.v_cache.cuda()
+    F.fa_cache_append(p.k_new.cuda(), p.v_new.cuda(), kc, vc, p.slot_mapping.cuda())
+    args = (p.q.cuda(), kc, vc, p.block_table.cuda(), p.ctx_lens.cuda(), p.q_lens.cuda())
+    n = F.fa_paged_attn_workspace_size(p.num_seqs, p.max_blocks_per_seq, p.Hq, p.Hkv, p.d, p.total_q)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    fills = [torch.zeros(n, dtype=torch.uint8), torch.full((n,), 255, dtype=torch.uint8),
+             torch.randint(0, 256, (n,), dtype=torch.uint8, generator=gen)]
+    outs = []
+    for fill in fills:
+        ws = fill.cuda()
+        for _ in range(2):  # the second call starts from the words the first one left
+            outs.append(F.fa_paged_attn(*args, causal=True, scale=p.scale, max_q_len=1, ws=ws))
+            assert F.fa_get_error() == F.FA_OK
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ref, _, _ = oracle_paged(p, bits(kc), bits(vc))
+    assert_parity(outs[0], ref, "decode, uncleared workspace")
