@@ -477,12 +477,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kt = U.kt0; kt < U.n_kt && ok; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
                 const int kidx = cons + 2 * it;
-                if (!mbar_wait_warp(&full[kidx % S], (kidx / S) & 1, lim_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
                 for (int s = 0; s < 2 && ok; ++s) {
+                    // P_s V of the previous tile goes out as soon as P_s is
+                    // ready; only the Q K^T after it waits for this tile's K
                     if (it > 0) {
                         if (s == 0 && !wait_v(prev_v, prev_kt, U.kv_len)) {
                             ok = false;
@@ -492,6 +489,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             ok = false;
                             break;
                         }
+                    }
+                    if (s == 0) {
+                        if (!mbar_wait_warp(&full[kidx % S], (kidx / S) & 1, lim_ns, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
                     if (lane == 0) {
                         issue_qk(s, kidx);
