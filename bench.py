@@ -488,6 +488,27 @@ def main():
                                  "achieved": tf5, "peak": tc_peak, "unit": "TFLOP/s",
                                  "frac": t_bound / (r5["ms"] * 1e-3), "traffic": None,
                                  "note": "frac = max(F/P_tc, B/BW) / measured time"}})
+        # rotary embedding fused with the append, at config 5's chunk size
+        rc = W.rope_case(21, 4096, 32, 8, 128, num_blocks=20000, max_pos=8704)
+        rq, rk, rv = rc.q.cuda(), rc.k.cuda(), rc.v.cuda()
+        rpos, rcs, rsm = rc.positions.cuda(), rc.cos_sin.cuda(), rc.slot_mapping.cuda()
+        rkc = torch.zeros(rc.num_blocks, 8, 16, 128, dtype=torch.bfloat16, device="cuda")
+        rvc, rqo = torch.zeros_like(rkc), torch.empty_like(rq)
+
+        def rope_step():
+            F.fa_cache_append_rope(rq, rk, rv, rpos, rcs, rkc, rvc, rsm, q_out=rqo)
+        rms, rl, _, _ = timer.run(rope_step, args.steps, args.warmup, ws)
+        rms = reduce_max(rms, ws)
+        rbytes = 2 * rq.numel() * 2 + 2 * (rk.numel() + rv.numel()) * 2 + rc.N * (128 * 4 + 8)
+        rgbs = rbytes / (rms * 1e-3) / 1e9
+        sec.append({"workload": "rotary embedding of q and k fused with the cache append: 4096 tokens, Hq=32 Hkv=8 "
+                                "d=128, positions U[0,8704), slots in a 20000-block pool",
+                    "metric": "fused append GB/s", "value": rgbs, "unit": "GB/s", "ms_per_step": rms,
+                    "gpu_launches": rl, "algorithmic_bytes": rbytes,
+                    "roofline": {"bound": "hbm", "achieved": rgbs, "peak": hbm, "unit": "GB/s", "frac": rgbs / hbm,
+                                 "traffic": None, "peak_source": f"{peak_src} hbm copy",
+                                 "kernel": "rope_append_kernel<false>"}})
+        del rq, rk, rv, rkc, rvc, rqo
         line["secondary"] = sec
 
     if rank == 0 and not args.no_cpu_baseline:

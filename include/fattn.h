@@ -119,6 +119,34 @@ fa_status fa_cache_append(const void* k, const void* v, void* k_cache, void* v_c
                           fa_dtype in_dtype, fa_stream_t stream);
 
 /*
+ * fa_cache_append_rope -- the append above fused with rotary position
+ * embeddings of queries and keys, in one launch.
+ * Passage: "Operator Fusion", fusion list (applying rotary position
+ * embeddings to queries and keys; updating the KV cache while transforming
+ * key and value tensors).  The pages name this fusion but not the rotation;
+ * the reading implemented is the rotate-half form: channel j (j < d/2) pairs
+ * with channel j + d/2 and both turn by the angle of table row positions[i]:
+ *   y_j = x_j c - x_{j+d/2} s,   y_{j+d/2} = x_{j+d/2} c + x_j s,
+ * c = cos_sin[pos][j], s = cos_sin[pos][d/2 + j], computed in fp32 and
+ * rounded once to bf16 (RNE).
+ *   q            [N, Hq, d] in `in_dtype`; rotated rows go to q_out bf16 [N, Hq, d]
+ *   k, v         [N, Hkv, d] in `in_dtype`; k rotated, v unchanged (fp32
+ *                values rounded to bf16, RNE), both written to slot
+ *                slot_mapping[i] as fa_cache_append places them
+ *   positions    int32 [N], 0 <= positions[i] < max_pos (else FA_ERR_BOUNDS is
+ *                recorded and token i is skipped entirely)
+ *   cos_sin      fp32 [max_pos, d], caller-owned (the angles are the caller's
+ *                choice of rotary base and position scaling)
+ *   slot_mapping int32 [N], as for fa_cache_append (s < 0: the query is still
+ *                rotated, the cache is not written)
+ * All pointers 16-byte aligned; d = 64 or 128.
+ */
+fa_status fa_cache_append_rope(const void* q, const void* k, const void* v, const int32_t* positions,
+                               const float* cos_sin, int max_pos, void* q_out, void* k_cache,
+                               void* v_cache, const int32_t* slot_mapping, int N, int Hq, int Hkv,
+                               int d, int num_blocks, fa_dtype in_dtype, fa_stream_t stream);
+
+/*
  * fa_paged_attn -- attention of packed queries against the paged cache.
  * Passage: "Paged Attention Kernels" (logical positions translated through
  * the block table; 16-token blocks); "FlashAttention-Style Kernels" (the

@@ -62,6 +62,8 @@ def _load():
         lib.ora_attention_rows.argtypes = [P, P, P, P, i, i, i, i, i, i, i, d, P, l, P, P, i]
         lib.ora_gather_kv.argtypes = [P, P, i, i, i, i, i, i, i, P]
         lib.ora_cache_append.argtypes = [P, P, P, i, i, i, i, i, P, P]
+        lib.ora_rope_f64.argtypes = [P, P, P, i, l, i, P]
+        lib.ora_rope_cache_append.argtypes = [P, P, P, P, P, i, P, i, i, i, i, i, i, P, P, P]
         lib.ora_paged_attention.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, i, d, P, P, i]
         lib.ora_paged_attention_rows.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, i, d,
                                                  P, l, P, P, i]
@@ -114,6 +116,18 @@ def to_bits(t) -> np.ndarray:
     if t.dtype == torch.float32:
         return bf16_rne(t)
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def to_f64(t) -> np.ndarray:
+    """Exact float64 values of an input tensor (bf16 bit patterns decoded, fp32 widened)."""
+    if isinstance(t, np.ndarray) and t.dtype == np.uint16:
+        return bits_to_f64(t)
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            return bits_to_f64(to_bits(t))
+        return t.numpy().astype(np.float64)
+    return np.ascontiguousarray(t, dtype=np.float64)
 
 
 def _i32(t) -> np.ndarray:
@@ -183,6 +197,36 @@ def cache_append(k, v, slot_mapping, k_cache_bits: np.ndarray, v_cache_bits: np.
     st = _load().ora_cache_append(_ptr(kb), _ptr(vb), _ptr(sm), N, Hkv, d, nb, bs, _ptr(kc), _ptr(vc))
     _check(st, "cache_append")
     return kc, vc
+
+
+def rope_f64(x, positions, cos_sin) -> np.ndarray:
+    """Rotate rows x f64 [nrows, d] (row i at table row positions[i]) with the
+    rotate-half rotary embedding of table cos_sin f32 [max_pos, d]; fp64 result."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    nrows, d = x.shape
+    pos = _i32(positions)
+    cs = _f32(cos_sin)
+    y = np.empty_like(x)
+    _check(_load().ora_rope_f64(_ptr(x), _ptr(pos), _ptr(cs), cs.shape[0], nrows, d, _ptr(y)), "rope_f64")
+    return y
+
+
+def rope_cache_append(q, k, v, positions, cos_sin, slot_mapping, k_cache_bits: np.ndarray,
+                      v_cache_bits: np.ndarray):
+    """Rotary embedding fused with the append: returns (q_out bits [N,Hq,d], new k cache, new v cache).
+    q and k are rotated from their exact values (bf16 or fp32); v is stored as bf16 (fp32 rounded, RNE)."""
+    qb, kb, vb = to_f64(q), to_f64(k), to_bits(v)
+    N, Hq, d = qb.shape
+    Hkv = kb.shape[1]
+    kc = np.ascontiguousarray(k_cache_bits, dtype=np.uint16).copy()
+    vc = np.ascontiguousarray(v_cache_bits, dtype=np.uint16).copy()
+    nb, _, bs, _ = kc.shape
+    pos, sm, cs = _i32(positions), _i32(slot_mapping), _f32(cos_sin)
+    qo = np.zeros(qb.shape, dtype=np.uint16)
+    st = _load().ora_rope_cache_append(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(pos), _ptr(cs), cs.shape[0], _ptr(sm), N,
+                                       Hq, Hkv, d, nb, bs, _ptr(qo), _ptr(kc), _ptr(vc))
+    _check(st, "rope_cache_append")
+    return qo, kc, vc
 
 
 def paged_attention(q, k_cache, v_cache, block_table, ctx_lens, q_lens, causal: bool, scale: float,

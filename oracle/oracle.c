@@ -23,7 +23,9 @@
  *   - section "Operator Fusion", fusion list item "updating the KV cache while
  *     transforming key and value tensors": the append writes each new token's
  *     K/V row into its cache slot (slot = block * 16 + offset), rounding fp32
- *     inputs to bf16.
+ *     inputs to bf16; with the list item "applying rotary position embeddings
+ *     to queries and keys", the fused variant rotates q and k first (the
+ *     rotation itself is a reading, stated at ora_rope_cache_append).
  *
  * Readings where the pages are silent (also listed in the design notes):
  *   - grouped-query attention: query head h reads kv head h / (Hq / Hkv);
@@ -403,6 +405,126 @@ int ora_cache_append(const uint16_t* k, const uint16_t* v, const int32_t* slot_m
             }
     }
     return ORA_OK;
+}
+
+/* ------------------------------------------------------ rotary + append -- */
+
+/*
+ * IEEE round-to-nearest-even of a double straight to bfloat16 (no
+ * intermediate binary32 rounding): keep 8 significant bits of the value.
+ */
+static uint16_t bf16_rne_double(double x)
+{
+    if (x != x)
+        return 0x7FC0u;
+    if (x == 0.0)
+        return signbit(x) ? 0x8000u : 0x0000u;
+    double ax = fabs(x), r;
+    if (ax < ldexp(1.0, -126)) {                /* bf16 subnormal range: spacing 2^-133 */
+        r = nearbyint(ax * ldexp(1.0, 133)) * ldexp(1.0, -133);
+    } else {
+        int e;
+        double m = frexp(ax, &e);               /* ax = m * 2^e, m in [1/2, 1) */
+        r = ldexp(nearbyint(ldexp(m, 8)), e - 8);
+    }
+    float f = r >= ldexp(1.0, 128) ? INFINITY : (float)r;   /* exact: r has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)((u >> 16) | (x < 0 ? 0x8000u : 0u));
+}
+
+/*
+ * Rotary position embedding of one d-channel row at table row `pos`.  The
+ * pages name the fusion ("Operator Fusion", fusion list: applying rotary
+ * position embeddings to queries and keys) but not the rotation; reading:
+ * the rotate-half form, channel j paired with channel j + d/2 (j < d/2) and
+ * turned by the angle whose cosine and sine sit at columns j and d/2 + j of
+ * the caller's table cos_sin [max_pos, d]:
+ *   y_j       = x_j cos - x_{j+d/2} sin
+ *   y_{j+d/2} = x_{j+d/2} cos + x_j sin        (fp64)
+ */
+static void rope_row(const double* x, const float* cs, int d, double* y)
+{
+    int h = d / 2;
+    for (int j = 0; j < h; ++j) {
+        double c = (double)cs[j], s = (double)cs[h + j];
+        y[j] = x[j] * c - x[h + j] * s;
+        y[h + j] = x[h + j] * c + x[j] * s;
+    }
+}
+
+/* rope_row over nrows rows (row i at table row pos[i]), fp64 in and out */
+int ora_rope_f64(const double* x, const int32_t* pos, const float* cos_sin, int max_pos, long nrows, int d,
+                 double* y)
+{
+    if (d <= 0 || d % 2)
+        return ORA_ERR_ARG;
+    for (long i = 0; i < nrows; ++i) {
+        if (pos[i] < 0 || pos[i] >= max_pos)
+            return ORA_ERR_BOUNDS;
+        rope_row(x + i * d, cos_sin + (long)pos[i] * d, d, y + i * d);
+    }
+    return ORA_OK;
+}
+
+/*
+ * Rotary embedding fused with the cache append ("Operator Fusion", fusion
+ * list: applying rotary position embeddings to queries and keys; updating
+ * the KV cache while transforming key and value tensors).  Token i sits at
+ * table row positions[i].  Its Hq query rows are rotated into q_out; its Hkv
+ * key rows are rotated and, with its unrotated value rows, written to slot
+ * slot_mapping[i] exactly as ora_cache_append places them (a negative slot
+ * skips the cache write only).  q and k come in as exact fp64 copies of the
+ * caller's values (bf16 or fp32), v as bf16 bits; rotated values are rounded
+ * once from fp64 to bf16 (RNE).
+ */
+int ora_rope_cache_append(const double* q, const double* k, const uint16_t* v, const int32_t* positions,
+                          const float* cos_sin, int max_pos, const int32_t* slot_mapping, int N, int Hq,
+                          int Hkv, int d, int num_blocks, int block_size, uint16_t* q_out,
+                          uint16_t* k_cache, uint16_t* v_cache)
+{
+    double* x = malloc(sizeof(double) * 2 * (size_t)d);
+    if (!x)
+        return ORA_ERR_NOMEM;
+    double* y = x + d;
+    int st = ORA_OK;
+    for (int i = 0; i < N && st == ORA_OK; ++i) {
+        int pos = positions[i];
+        if (pos < 0 || pos >= max_pos) {
+            st = ORA_ERR_BOUNDS;
+            break;
+        }
+        const float* cs = cos_sin + (long)pos * d;
+        for (int h = 0; h < Hq; ++h) {
+            long base = ((long)i * Hq + h) * d;
+            for (int c = 0; c < d; ++c)
+                x[c] = q[base + c];
+            rope_row(x, cs, d, y);
+            for (int c = 0; c < d; ++c)
+                q_out[base + c] = bf16_rne_double(y[c]);
+        }
+        long slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        if (slot >= (long)num_blocks * block_size) {
+            st = ORA_ERR_BOUNDS;
+            break;
+        }
+        long blk = slot / block_size, off = slot % block_size;
+        for (int h = 0; h < Hkv; ++h) {
+            long src = ((long)i * Hkv + h) * d;
+            long dst = ((blk * Hkv + h) * block_size + off) * d;
+            for (int c = 0; c < d; ++c)
+                x[c] = k[src + c];
+            rope_row(x, cs, d, y);
+            for (int c = 0; c < d; ++c) {
+                k_cache[dst + c] = bf16_rne_double(y[c]);
+                v_cache[dst + c] = v[src + c];
+            }
+        }
+    }
+    free(x);
+    return st;
 }
 
 /* ---------------------------------------------------- paged attention -- */

@@ -1,7 +1,8 @@
 // Memory-bound helper kernels of libfattn:
 //   * fused KV-cache append ("Fast Attention Kernels and Operator Fusion",
 //     section "Operator Fusion", fusion list: updating the KV cache while
-//     transforming key and value tensors);
+//     transforming key and value tensors), and its variant that also applies
+//     rotary position embeddings to queries and keys (same list);
 //   * fp32 -> bf16 staging cast;
 //   * block-table gather test hook ("Paged Attention Kernels": translate each
 //     logical position through the block table);
@@ -53,6 +54,99 @@ __global__ void __launch_bounds__(256) cache_append_kernel(const void* __restric
         }
         *reinterpret_cast<uint4*>(kc + dst) = kv4;
         *reinterpret_cast<uint4*>(vc + dst) = vv4;
+    }
+}
+
+// ------------------------------------------------------ rotary append ----
+// Rotate-half rotary embedding: channel j pairs with j + d/2 and turns by the
+// angle whose cosine / sine sit at columns j / d/2 + j of row `pos` of the
+// caller's fp32 table:  y_j = x_j c - x_{j+d/2} s,  y_{j+d/2} = x_{j+d/2} c + x_j s
+// (fp32, rounded once to bf16).  One thread handles 8 channel pairs of one
+// row: the 16-byte chunk at channel 8c and its partner chunk at d/2 + 8c.
+// Rows of a token: its Hq query rows (rotated into q_out), then its Hkv key
+// rows (rotated into the cache slot); the thread of a key chunk pair also
+// copies the same two chunks of the value row.
+template <bool kF32>
+__device__ __forceinline__ void load8(const void* base, long off, float (&x)[8]) {
+    if constexpr (kF32) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&y)[8]) {
+    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                      pack_bf16x2(y[6], y[7]));
+}
+
+template <bool kF32>
+__global__ void __launch_bounds__(256) rope_append_kernel(const void* __restrict__ q, const void* __restrict__ k,
+                                                          const void* __restrict__ v,
+                                                          const int32_t* __restrict__ positions,
+                                                          const float* __restrict__ cos_sin, int max_pos,
+                                                          uint16_t* __restrict__ q_out, uint16_t* __restrict__ kc,
+                                                          uint16_t* __restrict__ vc,
+                                                          const int32_t* __restrict__ slots, int N, int Hq, int Hkv,
+                                                          int d, int num_blocks, DevCtx ctx) {
+    const int half = d >> 1, cph = half >> 3;  // chunk pairs per row
+    const int rpt = Hq + Hkv;                   // rotated rows per token
+    const long total = (long)N * rpt * cph;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int c = (int)(idx % cph);
+        const long row = idx / cph;
+        const long tok = row / rpt;
+        const int r = (int)(row % rpt);
+        const int pos = __ldg(positions + tok);
+        if (pos < 0 || pos >= max_pos) {
+            raise_error(ctx, ERR_BOUNDS_BIT);
+            continue;
+        }
+        const bool is_q = r < Hq;
+        const int h = is_q ? r : r - Hq;
+        long dst = 0;
+        if (!is_q) {
+            const int slot = __ldg(slots + tok);
+            if (slot < 0) continue;
+            if (slot >= num_blocks * kBlock) {
+                raise_error(ctx, ERR_BOUNDS_BIT);
+                continue;
+            }
+            dst = (((long)(slot / kBlock) * Hkv + h) * kBlock + (slot % kBlock)) * d;
+        }
+        const long src = is_q ? (tok * Hq + h) * d : (tok * Hkv + h) * d;
+        float x1[8], x2[8], co[8], si[8], y1[8], y2[8];
+        load8<kF32>(is_q ? q : k, src + c * 8, x1);
+        load8<kF32>(is_q ? q : k, src + half + c * 8, x2);
+        const float4* cs = reinterpret_cast<const float4*>(cos_sin + (long)pos * d + c * 8);
+        const float4* sn = reinterpret_cast<const float4*>(cos_sin + (long)pos * d + half + c * 8);
+        const float4 c0 = __ldg(cs), c1 = __ldg(cs + 1), s0 = __ldg(sn), s1 = __ldg(sn + 1);
+        co[0] = c0.x; co[1] = c0.y; co[2] = c0.z; co[3] = c0.w; co[4] = c1.x; co[5] = c1.y; co[6] = c1.z; co[7] = c1.w;
+        si[0] = s0.x; si[1] = s0.y; si[2] = s0.z; si[3] = s0.w; si[4] = s1.x; si[5] = s1.y; si[6] = s1.z; si[7] = s1.w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            y1[i] = fmaf(x1[i], co[i], -(x2[i] * si[i]));
+            y2[i] = fmaf(x2[i], co[i], x1[i] * si[i]);
+        }
+        if (is_q) {
+            *reinterpret_cast<uint4*>(q_out + src + c * 8) = pack8(y1);
+            *reinterpret_cast<uint4*>(q_out + src + half + c * 8) = pack8(y2);
+        } else {
+            *reinterpret_cast<uint4*>(kc + dst + c * 8) = pack8(y1);
+            *reinterpret_cast<uint4*>(kc + dst + half + c * 8) = pack8(y2);
+            float v1[8], v2[8];
+            load8<kF32>(v, src + c * 8, v1);
+            load8<kF32>(v, src + half + c * 8, v2);
+            *reinterpret_cast<uint4*>(vc + dst + c * 8) = pack8(v1);
+            *reinterpret_cast<uint4*>(vc + dst + half + c * 8) = pack8(v2);
+        }
     }
 }
 
@@ -215,6 +309,39 @@ fa_status fa_debug_gather_kv(const void* cache, const int32_t* block_table, cons
     gather_kv_kernel<<<grid_for(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(cache), block_table, ctx_lens, static_cast<uint16_t*>(out), num_seqs,
         max_blocks_per_seq, num_blocks, Hkv, d, max_ctx, ctx);
+    st = cuda_status(cudaGetLastError());
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
+fa_status fa_cache_append_rope(const void* q, const void* k, const void* v, const int32_t* positions,
+                               const float* cos_sin, int max_pos, void* q_out, void* k_cache, void* v_cache,
+                               const int32_t* slot_mapping, int N, int Hq, int Hkv, int d, int num_blocks,
+                               fa_dtype in_dtype, fa_stream_t stream) {
+    set_launch_count(0);
+    if (N < 0 || Hq <= 0 || Hkv <= 0 || num_blocks < 0 || max_pos <= 0) return FA_ERR_INVALID_ARG;
+    if (in_dtype != FA_BF16 && in_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (N == 0) return FA_OK;
+    if (!q || !k || !v || !positions || !cos_sin || !q_out || !k_cache || !v_cache || !slot_mapping)
+        return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cos_sin) || !aligned16(q_out) ||
+        !aligned16(k_cache) || !aligned16(v_cache))
+        return FA_ERR_INVALID_ARG;
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    const long work = (long)N * (Hq + Hkv) * (d / 16);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FA_F32)
+        rope_append_kernel<true><<<grid_for(work, 256), 256, 0, s>>>(
+            q, k, v, positions, cos_sin, max_pos, static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(k_cache),
+            static_cast<uint16_t*>(v_cache), slot_mapping, N, Hq, Hkv, d, num_blocks, ctx);
+    else
+        rope_append_kernel<false><<<grid_for(work, 256), 256, 0, s>>>(
+            q, k, v, positions, cos_sin, max_pos, static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(k_cache),
+            static_cast<uint16_t*>(v_cache), slot_mapping, N, Hq, Hkv, d, num_blocks, ctx);
     st = cuda_status(cudaGetLastError());
     if (st == FA_OK) set_launch_count(1);
     return st;

@@ -25,6 +25,7 @@ EXPORTS = [
     "fa_status_string", "fa_prefill", "fa_prefill_masked_workspace_size", "fa_prefill_masked", "fa_stage_bf16",
     "fa_cache_append", "fa_paged_attn_workspace_size", "fa_paged_attn", "fa_get_error", "fa_debug_gather_kv",
     "fa_debug_set_wait_limit", "fa_debug_force_timeout", "fa_last_launch_count", "fa_paged_attn_noalloc",
+    "fa_cache_append_rope",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
@@ -53,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "fa_get_error": (I, [P]),
         "fa_debug_gather_kv": (I, [P, P, P, P, I, I, I, I, I, I, P]),
         "fa_debug_set_wait_limit": (None, [ctypes.c_ulonglong]),
+        "fa_cache_append_rope": (I, [P, P, P, P, P, I, P, P, P, P, I, I, I, I, I, I, P]),
         "fa_debug_force_timeout": (None, [I]),
         "fa_paged_attn_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P]),
         "fa_last_launch_count": (I, []),
@@ -172,6 +174,32 @@ def fa_cache_append(k, v, k_cache, v_cache, slot_mapping, stream=None):
     dt = FA_F32 if k.dtype == torch.float32 else FA_BF16
     _check(_lib.fa_cache_append(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hkv, d,
                                 k_cache.shape[0], dt, _stream(stream)), "fa_cache_append")
+
+
+def fa_cache_append_rope(q, k, v, positions, cos_sin, k_cache, v_cache, slot_mapping, q_out=None, stream=None):
+    """Rotary embedding of q [N,Hq,d] and k [N,Hkv,d] at table rows positions[N]
+    (cos_sin fp32 [max_pos, d]: cosines then sines), fused with the cache
+    append of the rotated k and of v; returns the rotated queries (bf16)."""
+    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be bf16 or all fp32")
+    _need(q, "q", q.dtype, 3)
+    _need(k, "k", q.dtype, 3)
+    _need(v, "v", q.dtype, 3)
+    _need(positions, "positions", torch.int32, 1)
+    _need(cos_sin, "cos_sin", torch.float32, 2)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    N, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if q_out is None:
+        q_out = torch.empty(N, Hq, d, dtype=torch.bfloat16, device=q.device)
+    _need(q_out, "q_out", torch.bfloat16, 3)
+    dt = FA_F32 if q.dtype == torch.float32 else FA_BF16
+    _check(_lib.fa_cache_append_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(cos_sin), cos_sin.shape[0],
+                                     _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hq, Hkv, d,
+                                     k_cache.shape[0], dt, _stream(stream)), "fa_cache_append_rope")
+    return q_out
 
 
 def fa_paged_attn_workspace_size(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q) -> int:

@@ -70,6 +70,17 @@ def test_host_validation(fattn):
     assert lib.fa_cache_append(dummy, dummy, dummy, dummy, dummy, 4, 2, 64, 8, 7, None) == fattn.FA_ERR_INVALID_ARG
     assert lib.fa_cache_append(dummy, dummy, dummy, dummy, dummy, 4, 2, 80, 8, 0, None) == fattn.FA_ERR_UNSUPPORTED
     assert lib.fa_cache_append(None, None, None, None, None, 0, 2, 64, 8, 0, None) == fattn.FA_OK
+    # fused rotary append: bad sizes, dtype code, head dim, table, alignment
+    args = lambda **kw: [kw.get(n, dummy) for n in ("q", "k", "v", "pos", "cs")] + [kw.get("max_pos", 8)] + \
+        [kw.get(n, dummy) for n in ("qo", "kc", "vc", "sm")] + [kw.get("N", 4), 4, 2, kw.get("d", 64), 8,
+                                                                 kw.get("dt", 0), None]
+    assert lib.fa_cache_append_rope(*args(N=-1)) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_cache_append_rope(*args(dt=7)) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_cache_append_rope(*args(max_pos=0)) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_cache_append_rope(*args(d=80)) == fattn.FA_ERR_UNSUPPORTED
+    assert lib.fa_cache_append_rope(*args(cs=None)) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_cache_append_rope(*args(qo=P(4096 + 8))) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_cache_append_rope(*args(N=0, q=None, k=None)) == fattn.FA_OK
     # masked prefill workspace
     assert lib.fa_prefill_masked_workspace_size(16384) >= 128 * 128 + 128 * 4
     assert lib.fa_prefill_masked(dummy, dummy, dummy, dummy, dummy, 1, 300, 4, 2, 64, 0, 0.1, None, dummy, 10,

@@ -366,3 +366,82 @@ def test_mask_tile_classes_recover_planted_map():
     assert np.array_equal(got, planted)
     assert np.array_equal(oracle.mask_tile_classes(W.make_mask("causal_inf", 256, 256)),
                           np.array([[2, 0], [1, 2]], np.uint8))
+
+
+# ---------------------------------------------------- rotary + append -----
+# The rotation is a reading (rotate-half pairing, caller-given cos/sin table);
+# these pin the oracle's arithmetic to properties of that rotation that do
+# not depend on its own code: a hand-worked case, the identity, norm
+# preservation, the relative-position property and composition, plus the
+# single rounding from fp64 to bf16.
+
+def _bits(a):
+    return oracle.bf16_rne(np.asarray(a, np.float32))
+
+
+def test_rope_hand_case_quarter_and_half_turn():
+    # d = 4: pairs (0, 2) and (1, 3); pair 0 turned by +90 degrees, pair 1 by 180
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    cs = np.array([[0.0, -1.0, 1.0, 0.0]], np.float32)  # cos0, cos1, sin0, sin1
+    y = oracle.rope_f64(x, [0], cs)
+    assert np.array_equal(y, [[-3.0, -2.0, 1.0, -4.0]])
+
+
+def test_rope_zero_angle_is_the_plain_append():
+    c = W.rope_case(11, 40, 4, 2, 64, num_blocks=8, max_pos=32, skip_every=7)
+    ident = torch.cat([torch.ones(32, 32), torch.zeros(32, 32)], dim=1)
+    z = np.zeros((8, 2, 16, 64), np.uint16)
+    qo, kc, vc = oracle.rope_cache_append(c.q, c.k, c.v, c.positions, ident, c.slot_mapping, z, z)
+    ek, ev = oracle.cache_append(c.k, c.v, c.slot_mapping, z, z)
+    assert np.array_equal(qo, oracle.to_bits(c.q))
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+
+
+def test_rope_preserves_pair_norms():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((64, 128))
+    tab = W.rope_table(4096, 128)
+    pos = rng.integers(0, 4096, 64)
+    y = oracle.rope_f64(x, pos, tab)
+    n0 = x[:, :64] ** 2 + x[:, 64:] ** 2
+    n1 = y[:, :64] ** 2 + y[:, 64:] ** 2
+    # the stored table is cos/sin rounded to fp32, so c^2 + s^2 = 1 within ~1e-7
+    assert np.allclose(n1, n0, rtol=3e-7, atol=1e-12)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((1, 128))
+    k = rng.standard_normal((1, 128))
+    tab = W.rope_table(4096, 128)
+
+    def score(m, n):
+        return float((oracle.rope_f64(q, [m], tab) @ oracle.rope_f64(k, [n], tab).T)[0, 0])
+
+    for m, n, shift in [(10, 3, 100), (700, 650, 2000), (5, 5, 3000)]:
+        assert abs(score(m, n) - score(m + shift, n + shift)) <= 1e-4 * (1.0 + abs(score(m, n)))
+    assert abs(score(40, 3) - score(3, 40)) > 1e-3  # not symmetric: it is the signed offset that counts
+
+
+def test_rope_rotations_compose():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((3, 64))
+    tab = W.rope_table(2048, 64)
+    a, b = [17, 400, 900], [5, 600, 1000]
+    twice = oracle.rope_f64(oracle.rope_f64(x, a, tab), b, tab)
+    once = oracle.rope_f64(x, np.add(a, b), tab)
+    assert np.allclose(twice, once, rtol=0, atol=2e-5)
+
+
+def test_rope_rounds_once_from_fp64():
+    # y0 = 1 * (1 + 2^-8) - 2^-15 * (-2^-15) = 1 + 2^-8 + 2^-30: just above the
+    # midpoint of bf16 1.0 and 1.0078125, so it rounds up.  Rounding through
+    # fp32 first would lose the 2^-30 and round the tie to even (1.0).
+    q = torch.tensor([[[1.0, 0.5, 2.0 ** -15, 0.25]]]).to(torch.bfloat16)
+    kv = torch.zeros(1, 1, 4, dtype=torch.bfloat16)
+    cs = np.array([[1 + 2.0 ** -8, 1.0, -2.0 ** -15, 0.0]], np.float32)
+    z = np.zeros((1, 1, 16, 4), np.uint16)
+    qo, _, _ = oracle.rope_cache_append(q, kv, kv, [0], cs, [0], z, z)
+    assert qo[0, 0, 0] == 0x3F81           # 1.0078125
+    assert qo[0, 0, 2] == _bits([2.0 ** -23])[0]
+    assert qo[0, 0, 1] == _bits([0.5])[0] and qo[0, 0, 3] == _bits([0.25])[0]

@@ -45,7 +45,7 @@ _CHUNK = 1 << 22
 BLOCK_SIZE = 16
 
 # stream ids (one per tensor role)
-S_Q, S_K, S_V, S_CTX, S_QLEN, S_PERM, S_KC, S_VC, S_KNEW, S_VNEW, S_MISC = range(1, 12)
+S_Q, S_K, S_V, S_CTX, S_QLEN, S_PERM, S_KC, S_VC, S_KNEW, S_VNEW, S_MISC, S_POS = range(1, 13)
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -392,3 +392,47 @@ def attention_flops(Tq: int, Tk: int, d: int, heads: int, causal: bool) -> float
     else:
         pairs = Tq * Tk
     return 4.0 * d * heads * pairs
+
+
+# ------------------------------------------------------ rotary + append ----
+def rope_table(max_pos: int, d: int, theta: float = 1.0e6) -> torch.Tensor:
+    """Caller-side table of the fused rotary append, float32 [max_pos, d]:
+    row p holds cos(p * theta**(-2j/d)) at column j and the sine at column
+    d/2 + j (j < d/2), angles in float64, stored as float32.  theta = 1e6 is
+    the rotary base of the Qwen2.5 models the pages' example serves."""
+    j = np.arange(d // 2, dtype=np.float64)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * theta ** (-2.0 * j / d)[None, :]
+    return torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+
+
+@dataclass
+class RopeCase:
+    name: str
+    q: torch.Tensor          # [N, Hq, d]
+    k: torch.Tensor          # [N, Hkv, d]
+    v: torch.Tensor          # [N, Hkv, d]
+    positions: torch.Tensor  # int32 [N]
+    slot_mapping: torch.Tensor  # int32 [N]
+    cos_sin: torch.Tensor    # float32 [max_pos, d]
+    num_blocks: int
+
+    @property
+    def N(self) -> int:
+        return self.q.shape[0]
+
+
+def rope_case(seed: int, N: int, Hq: int, Hkv: int, d: int, num_blocks: int, max_pos: int,
+              dtype=torch.bfloat16, skip_every: int = 0, name: str = "rope") -> RopeCase:
+    """N new tokens: q, k, v ~ N(0,1) (streams S_Q, S_KNEW, S_VNEW); positions
+    uniform in [0, max_pos) (stream S_POS); distinct cache slots drawn as a
+    permutation of the pool (stream S_PERM); with skip_every > 0 every
+    skip_every-th token gets slot -1 (not written)."""
+    q = normal_tensor(seed, S_Q, (N, Hq, d), dtype)
+    k = normal_tensor(seed, S_KNEW, (N, Hkv, d), dtype)
+    v = normal_tensor(seed, S_VNEW, (N, Hkv, d), dtype)
+    pos = uniform_int(seed, S_POS, 0, max_pos - 1, N).astype(np.int32)
+    slots = permutation(seed, S_PERM, num_blocks * BLOCK_SIZE)[:N].astype(np.int32)
+    if skip_every:
+        slots[::skip_every] = -1
+    return RopeCase(name, q, k, v, torch.from_numpy(pos), torch.from_numpy(slots), rope_table(max_pos, d),
+                    num_blocks)
