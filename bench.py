@@ -286,6 +286,50 @@ def bench_paged(F, timer, p, steps, warmup, ws, with_append=False):
     return dict(ms=ms, launches=launches, wall=wall)
 
 
+def bench_decode_graph(F, p, warmup, n_steps=200):
+    """Host submission cost of a decode step: n_steps steps issued back to
+    back (no L2 flush: this measures launch overhead, not bandwidth), once as
+    eager calls through the binding (Python + C ABI + three kernel launches
+    per step) and once as replays of the step captured by fa_decode_graph_*.
+    Wall time per step (host clock around the loop, synchronised) and device
+    time per step (CUDA events around the loop)."""
+    t = paged_setup(F, p)
+    kn, vn, sm = p.k_new.cuda(), p.v_new.cuda(), p.slot_mapping.cuda()
+    mq = int(p.q_lens.max())
+
+    def eager():
+        F.fa_cache_append(kn, vn, t["kc"], t["vc"], sm)
+        F.fa_paged_attn(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["ql"], causal=True, scale=p.scale,
+                        out=t["out"], max_q_len=mq, ws=t["ws"])
+    eager()
+    g = F.DecodeGraph(t["q"], t["kc"], t["vc"], t["bt"], t["ctx"], t["ql"], t["out"], t["ws"], k_new=kn, v_new=vn,
+                      slot_mapping=sm, scale=p.scale, max_q_len=mq)
+    res = {}
+    for name, fn in (("eager", eager), ("graph", g.replay)):
+        for _ in range(max(3, warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record()
+        for _ in range(n_steps):
+            fn()
+        b.record()
+        b.synchronize()
+        wall = (time.perf_counter() - t0) / n_steps * 1e6
+        res[name] = (wall, a.elapsed_time(b) / n_steps * 1e3)
+    assert F.fa_get_error() == F.FA_OK
+    kernels = g.kernel_count
+    g.close()
+    return {"workload": "config 3 decode step: append of the 64 new tokens + paged attention, "
+                        f"{n_steps} steps submitted back to back (L2 not flushed)",
+            "metric": "decode step wall time", "unit": "us", "higher_is_better": False,
+            "value": res["graph"][0], "eager_wall_us": res["eager"][0], "graph_wall_us": res["graph"][0],
+            "eager_device_us": res["eager"][1], "graph_device_us": res["graph"][1],
+            "launch_overhead_share": (res["eager"][0] - res["graph"][0]) / res["eager"][0],
+            "kernels_per_step": kernels}
+
+
 # ----------------------------------------------------------- cpu baseline ---
 def oracle_sample_c2(batches: int = 1):
     """Bounded sample of config 2 for the CPU oracle: the first `batches`
@@ -509,6 +553,9 @@ def main():
                                  "traffic": None, "peak_source": f"{peak_src} hbm copy",
                                  "kernel": "rope_append_kernel<false>"}})
         del rq, rk, rv, rkc, rvc, rqo
+        # config 3 decode step (append of each sequence's new token + paged
+        # attention), submitted back to back: eager calls vs one CUDA-graph replay
+        sec.append(bench_decode_graph(F, W.config3(), args.warmup))
         line["secondary"] = sec
 
     if rank == 0 and not args.no_cpu_baseline:

@@ -218,6 +218,42 @@ fa_status fa_paged_attn_noalloc(const void* q, const void* k_cache, const void* 
                                 int max_q_len, fa_stream_t stream);
 
 /*
+ * fa_decode_graph_* -- a decode step recorded once as a CUDA graph and
+ * replayed with one submission.
+ * Passage: "Fusion and CUDA Graphs with torch.compile" (a CUDA Graph records
+ * the sequence of GPU operations and replays it with one CPU submission,
+ * reducing launch overhead; replay requires stable memory addresses and
+ * compatible shapes; most useful for repeated small-batch work such as
+ * decode).
+ * _create captures fa_cache_append (skipped when n_new == 0) followed by
+ * fa_paged_attn with exactly these arguments on a private stream and
+ * instantiates the graph; nothing runs.  Every pointer and size is fixed from
+ * then on: between replays the caller rewrites buffer contents only (new
+ * rows, slot mapping, block table, context lengths, which the kernels read on
+ * the device); a change of any size needs a new graph.  Argument meaning,
+ * layout and errors are those of the two captured calls (their status is
+ * returned, and no graph is made); FA_ERR_CUDA if capture or instantiation
+ * fails.  Call the two entry points once eagerly on the same device before
+ * the first capture: first-use setup inside the library is not capturable.
+ * _launch replays on `stream` (asynchronous; fa_get_error reports device-side
+ * errors as for the eager calls).  _kernel_count is the number of kernels one
+ * replay runs.  _destroy frees the graph (NULL is ignored).  The handle is
+ * not thread-safe; replays of one handle must not overlap on the GPU.
+ */
+typedef struct fa_decode_graph fa_decode_graph;
+fa_status fa_decode_graph_create(fa_decode_graph** out, const void* k_new, const void* v_new,
+                                 const int32_t* slot_mapping, int n_new, fa_dtype in_dtype,
+                                 const void* q, void* k_cache, void* v_cache,
+                                 const int32_t* block_table, const int32_t* ctx_lens,
+                                 const int32_t* q_lens, void* attn_out, int num_seqs,
+                                 int max_blocks_per_seq, int num_blocks, int Hq, int Hkv, int d,
+                                 int causal, float scale, int total_q, int max_q_len, void* ws,
+                                 size_t ws_bytes);
+fa_status fa_decode_graph_launch(fa_decode_graph* graph, fa_stream_t stream);
+int fa_decode_graph_kernel_count(const fa_decode_graph* graph);
+void fa_decode_graph_destroy(fa_decode_graph* graph);
+
+/*
  * fa_get_error -- synchronises `stream`, then returns and clears the current
  * device's error word: FA_OK, FA_ERR_BOUNDS or FA_ERR_TIMEOUT (FA_ERR_BOUNDS
  * when both were recorded), or FA_ERR_CUDA if synchronisation itself failed.

@@ -25,7 +25,8 @@ EXPORTS = [
     "fa_status_string", "fa_prefill", "fa_prefill_masked_workspace_size", "fa_prefill_masked", "fa_stage_bf16",
     "fa_cache_append", "fa_paged_attn_workspace_size", "fa_paged_attn", "fa_get_error", "fa_debug_gather_kv",
     "fa_debug_set_wait_limit", "fa_debug_force_timeout", "fa_last_launch_count", "fa_paged_attn_noalloc",
-    "fa_cache_append_rope",
+    "fa_cache_append_rope", "fa_decode_graph_create", "fa_decode_graph_launch", "fa_decode_graph_kernel_count",
+    "fa_decode_graph_destroy",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
@@ -55,6 +56,11 @@ def _load() -> ctypes.CDLL:
         "fa_debug_gather_kv": (I, [P, P, P, P, I, I, I, I, I, I, P]),
         "fa_debug_set_wait_limit": (None, [ctypes.c_ulonglong]),
         "fa_cache_append_rope": (I, [P, P, P, P, P, I, P, P, P, P, I, I, I, I, I, I, P]),
+        "fa_decode_graph_create": (I, [P, P, P, P, I, I, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                       ctypes.c_float, I, I, P, ctypes.c_size_t]),
+        "fa_decode_graph_launch": (I, [P, P]),
+        "fa_decode_graph_kernel_count": (I, [P]),
+        "fa_decode_graph_destroy": (None, [P]),
         "fa_debug_force_timeout": (None, [I]),
         "fa_paged_attn_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P]),
         "fa_last_launch_count": (I, []),
@@ -200,6 +206,49 @@ def fa_cache_append_rope(q, k, v, positions, cos_sin, k_cache, v_cache, slot_map
                                      _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hq, Hkv, d,
                                      k_cache.shape[0], dt, _stream(stream)), "fa_cache_append_rope")
     return q_out
+
+
+class DecodeGraph:
+    """fa_decode_graph_*: the append of k_new/v_new (if given) plus paged
+    attention, captured once with these tensors and replayed with one
+    submission.  Keep every tensor alive and rewrite contents only."""
+
+    def __init__(self, q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, ws, *, k_new=None, v_new=None,
+                 slot_mapping=None, causal: bool = True, scale: float | None = None, max_q_len: int | None = None):
+        total_q, Hq, d = q.shape
+        num_blocks, Hkv, _, _ = k_cache.shape
+        num_seqs, mbps = block_table.shape
+        n_new, dt = 0, FA_BF16
+        if k_new is not None:
+            n_new = k_new.shape[0]
+            dt = FA_F32 if k_new.dtype == torch.float32 else FA_BF16
+        self._keep = (q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, ws, k_new, v_new, slot_mapping)
+        h = ctypes.c_void_p()
+        _check(_lib.fa_decode_graph_create(
+            ctypes.byref(h), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n_new, dt, _ptr(q), _ptr(k_cache),
+            _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), _ptr(q_lens), _ptr(out), num_seqs, mbps, num_blocks,
+            Hq, Hkv, d, int(causal), float(scale if scale is not None else 1.0 / math.sqrt(d)), total_q,
+            int(max_q_len if max_q_len is not None else total_q), _ptr(ws), ws.numel() * ws.element_size()),
+            "fa_decode_graph_create")
+        self._h = h
+
+    @property
+    def kernel_count(self) -> int:
+        return int(_lib.fa_decode_graph_kernel_count(self._h))
+
+    def replay(self, stream=None):
+        _check(_lib.fa_decode_graph_launch(self._h, _stream(stream)), "fa_decode_graph_launch")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.fa_decode_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def fa_paged_attn_workspace_size(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q) -> int:

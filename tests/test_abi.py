@@ -81,6 +81,16 @@ def test_host_validation(fattn):
     assert lib.fa_cache_append_rope(*args(cs=None)) == fattn.FA_ERR_INVALID_ARG
     assert lib.fa_cache_append_rope(*args(qo=P(4096 + 8))) == fattn.FA_ERR_INVALID_ARG
     assert lib.fa_cache_append_rope(*args(N=0, q=None, k=None)) == fattn.FA_OK
+    # decode graph: missing handle slot, negative token count, null handle
+    gargs = [None] * 3 + [0, 0] + [None] * 7 + [1, 4, 8, 4, 2, 64, 1, 0.1, 1, 1, None, 0]
+    assert lib.fa_decode_graph_create(None, *gargs) == fattn.FA_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    gargs[3] = -1
+    assert lib.fa_decode_graph_create(ctypes.byref(h), *gargs) == fattn.FA_ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.fa_decode_graph_launch(None, None) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_decode_graph_kernel_count(None) == 0
+    lib.fa_decode_graph_destroy(None)
     # masked prefill workspace
     assert lib.fa_prefill_masked_workspace_size(16384) >= 128 * 128 + 128 * 4
     assert lib.fa_prefill_masked(dummy, dummy, dummy, dummy, dummy, 1, 300, 4, 2, 64, 0, 0.1, None, dummy, 10,
