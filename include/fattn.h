@@ -55,7 +55,8 @@ typedef enum {
     FA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
     FA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (read by fa_get_error) */
     FA_ERR_BOUNDS = 5,      /* device-side index check failed (read by fa_get_error) */
-    FA_ERR_WORKSPACE = 6    /* workspace missing or smaller than the size query says */
+    FA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than the size query says */
+    FA_ERR_NO_BLOCKS = 7    /* the block pool has no free block left */
 } fa_status;
 
 typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
@@ -216,6 +217,60 @@ fa_status fa_paged_attn_noalloc(const void* q, const void* k_cache, const void* 
                                 int max_blocks_per_seq, int num_blocks, int Hq, int Hkv, int d,
                                 int block_size, int causal, float scale, int total_q,
                                 int max_q_len, fa_stream_t stream);
+
+/*
+ * fa_pool_* -- host-side pool of cache blocks with prefix sharing.
+ * Passage: "Paged Attention Kernels" (a logical sequence is a block table;
+ * blocks are allocated on demand, returned to a pool when a request ends,
+ * and shared when sequences have a common prefix).
+ * Bookkeeping only (no device memory is touched; all arrays are host
+ * memory).  Blocks are ids 0 .. num_blocks-1 of the caches fa_cache_append
+ * writes; every block has a reference count, and a block shared by several
+ * sequences is always full, so it is never written again.
+ *   _create      pool of num_blocks blocks; tables are max_blocks_per_seq wide
+ *   _add_seq     new empty sequence, id in *seq
+ *   _fork        new sequence *child holding the first prefix_len tokens of
+ *                `parent` (0 <= prefix_len <= parent's length): the full blocks
+ *                of the prefix are shared; when prefix_len % 16 != 0 the block
+ *                with the prefix tail is copied on write -- the child gets a
+ *                fresh block and (*copy_src, *copy_dst) name the copy the caller
+ *                must run (fa_copy_blocks) before writing to the child; else
+ *                both are -1
+ *   _append      slots for n new tokens of `seq` (slots[i] = block * 16 +
+ *                offset, for fa_cache_append), taking blocks from the free
+ *                list as needed; all or nothing
+ *   _release     ends a sequence; its blocks' counts drop and blocks reaching
+ *                0 return to the free list; the id may be reused
+ *   _tables      block-table rows [n, max_blocks_per_seq] (unused entries -1,
+ *                never read by the kernels) and lengths of n sequences
+ *   _num_free, _refcount, _seq_len  queries (-1 on a bad argument)
+ * Errors: FA_ERR_INVALID_ARG (bad id, length beyond max_blocks_per_seq * 16,
+ * null pointer), FA_ERR_NO_BLOCKS (no free block; the pool is unchanged; also
+ * host memory for the pool itself).  A pool is thread-safe.
+ */
+typedef struct fa_block_pool fa_block_pool;
+fa_status fa_pool_create(fa_block_pool** pool, int num_blocks, int max_blocks_per_seq);
+void fa_pool_destroy(fa_block_pool* pool);
+fa_status fa_pool_add_seq(fa_block_pool* pool, int* seq);
+fa_status fa_pool_fork(fa_block_pool* pool, int parent, int prefix_len, int* child, int* copy_src,
+                       int* copy_dst);
+fa_status fa_pool_append(fa_block_pool* pool, int seq, int n, int32_t* slots);
+fa_status fa_pool_release(fa_block_pool* pool, int seq);
+fa_status fa_pool_tables(const fa_block_pool* pool, const int* seqs, int n, int32_t* table,
+                         int32_t* ctx_lens);
+int fa_pool_num_free(const fa_block_pool* pool);
+int fa_pool_refcount(const fa_block_pool* pool, int block);
+int fa_pool_seq_len(const fa_block_pool* pool, int seq);
+
+/*
+ * fa_copy_blocks -- device side of the pool's copy on write: for each of the
+ * n pairs (device int32 [n, 2]) copies block pairs[i][0] onto pairs[i][1] in
+ * both caches (bf16 [num_blocks, Hkv, 16, d], 16-byte aligned).  A block id
+ * outside [0, num_blocks) records FA_ERR_BOUNDS and that pair is skipped.
+ * Exact (bit copy).
+ */
+fa_status fa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int n, int Hkv, int d,
+                         int num_blocks, fa_stream_t stream);
 
 /*
  * fa_decode_graph_* -- a decode step recorded once as a CUDA graph and

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libfattn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "cache_ops.cu", "paged.cu", "attn_tc.cu", "graph.cu"]
+SOURCES = ["api.cu", "cache_ops.cu", "paged.cu", "attn_tc.cu", "graph.cu", "block_pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 
@@ -42,7 +42,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]

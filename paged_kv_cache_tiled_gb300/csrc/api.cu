@@ -125,6 +125,7 @@ const char* fa_status_string(fa_status s) {
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
         case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS";
         case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+        case FA_ERR_NO_BLOCKS: return "FA_ERR_NO_BLOCKS";
     }
     return "FA_ERR_UNKNOWN";
 }

@@ -150,6 +150,28 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const void* __restrict
     }
 }
 
+// -------------------------------------------------------- block copy ------
+// Copy-on-write for the block pool: pair i copies physical block
+// pairs[2i] onto pairs[2i+1] in both caches (Hkv * 16 * d bf16 each),
+// 16 bytes per thread.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
+                                                          const int32_t* __restrict__ pairs, int n, int Hkv, int d,
+                                                          int num_blocks, DevCtx ctx) {
+    const long per = (long)Hkv * kBlock * d / 8;  // 16-byte chunks per block
+    const long total = (long)n * per;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const long i = idx / per, c = idx % per;
+        const int src = __ldg(pairs + 2 * i), dst = __ldg(pairs + 2 * i + 1);
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            raise_error(ctx, ERR_BOUNDS_BIT);
+            continue;
+        }
+        const long so = (long)src * per + c, dof = (long)dst * per + c;
+        reinterpret_cast<uint4*>(kc)[dof] = reinterpret_cast<const uint4*>(kc)[so];
+        reinterpret_cast<uint4*>(vc)[dof] = reinterpret_cast<const uint4*>(vc)[so];
+    }
+}
+
 // ------------------------------------------------------------- stage ------
 __global__ void __launch_bounds__(256) stage_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst,
                                                          size_t n) {
@@ -342,6 +364,25 @@ fa_status fa_cache_append_rope(const void* q, const void* k, const void* v, cons
         rope_append_kernel<false><<<grid_for(work, 256), 256, 0, s>>>(
             q, k, v, positions, cos_sin, max_pos, static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(k_cache),
             static_cast<uint16_t*>(v_cache), slot_mapping, N, Hq, Hkv, d, num_blocks, ctx);
+    st = cuda_status(cudaGetLastError());
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
+fa_status fa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int n, int Hkv, int d, int num_blocks,
+                         fa_stream_t stream) {
+    set_launch_count(0);
+    if (n < 0 || Hkv <= 0 || num_blocks < 0) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (n == 0) return FA_OK;
+    if (!k_cache || !v_cache || !pairs || !aligned16(k_cache) || !aligned16(v_cache)) return FA_ERR_INVALID_ARG;
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    const long work = (long)n * Hkv * kBlock * d / 8;
+    copy_blocks_kernel<<<grid_for(work, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache), pairs, n, Hkv, d, num_blocks, ctx);
     st = cuda_status(cudaGetLastError());
     if (st == FA_OK) set_launch_count(1);
     return st;

@@ -12,12 +12,14 @@ import ctypes
 import math
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfattn.so")
 
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BOUNDS, FA_ERR_WORKSPACE = range(7)
+(FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_BOUNDS, FA_ERR_WORKSPACE,
+ FA_ERR_NO_BLOCKS) = range(8)
 FA_BF16, FA_F32 = 0, 1
 
 # every symbol declared in include/fattn.h
@@ -26,7 +28,9 @@ EXPORTS = [
     "fa_cache_append", "fa_paged_attn_workspace_size", "fa_paged_attn", "fa_get_error", "fa_debug_gather_kv",
     "fa_debug_set_wait_limit", "fa_debug_force_timeout", "fa_last_launch_count", "fa_paged_attn_noalloc",
     "fa_cache_append_rope", "fa_decode_graph_create", "fa_decode_graph_launch", "fa_decode_graph_kernel_count",
-    "fa_decode_graph_destroy",
+    "fa_decode_graph_destroy", "fa_pool_create", "fa_pool_destroy", "fa_pool_add_seq", "fa_pool_fork",
+    "fa_pool_append", "fa_pool_release", "fa_pool_tables", "fa_pool_num_free", "fa_pool_refcount", "fa_pool_seq_len",
+    "fa_copy_blocks",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
@@ -61,6 +65,17 @@ def _load() -> ctypes.CDLL:
         "fa_decode_graph_launch": (I, [P, P]),
         "fa_decode_graph_kernel_count": (I, [P]),
         "fa_decode_graph_destroy": (None, [P]),
+        "fa_pool_create": (I, [P, I, I]),
+        "fa_pool_destroy": (None, [P]),
+        "fa_pool_add_seq": (I, [P, P]),
+        "fa_pool_fork": (I, [P, I, I, P, P, P]),
+        "fa_pool_append": (I, [P, I, I, P]),
+        "fa_pool_release": (I, [P, I]),
+        "fa_pool_tables": (I, [P, P, I, P, P]),
+        "fa_pool_num_free": (I, [P]),
+        "fa_pool_refcount": (I, [P, I]),
+        "fa_pool_seq_len": (I, [P, I]),
+        "fa_copy_blocks": (I, [P, P, P, I, I, I, I, P]),
         "fa_debug_force_timeout": (None, [I]),
         "fa_paged_attn_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P]),
         "fa_last_launch_count": (I, []),
@@ -206,6 +221,76 @@ def fa_cache_append_rope(q, k, v, positions, cos_sin, k_cache, v_cache, slot_map
                                      _ptr(q_out), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hq, Hkv, d,
                                      k_cache.shape[0], dt, _stream(stream)), "fa_cache_append_rope")
     return q_out
+
+
+class BlockPool:
+    """fa_pool_*: host-side block pool with reference counts and prefix
+    sharing.  Methods mirror the C functions; arrays are numpy."""
+
+    def __init__(self, num_blocks: int, max_blocks_per_seq: int):
+        h = ctypes.c_void_p()
+        _check(_lib.fa_pool_create(ctypes.byref(h), num_blocks, max_blocks_per_seq), "fa_pool_create")
+        self._h, self.num_blocks, self.max_blocks_per_seq = h, num_blocks, max_blocks_per_seq
+
+    def add_seq(self) -> int:
+        s = ctypes.c_int()
+        _check(_lib.fa_pool_add_seq(self._h, ctypes.byref(s)), "fa_pool_add_seq")
+        return s.value
+
+    def fork(self, parent: int, prefix_len: int):
+        """Returns (child, (copy_src, copy_dst)) with (-1, -1) when no copy is needed."""
+        c, a, b = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check(_lib.fa_pool_fork(self._h, parent, prefix_len, ctypes.byref(c), ctypes.byref(a), ctypes.byref(b)),
+               "fa_pool_fork")
+        return c.value, (a.value, b.value)
+
+    def append(self, seq: int, n: int) -> np.ndarray:
+        slots = np.zeros(max(n, 1), np.int32)
+        _check(_lib.fa_pool_append(self._h, seq, n, slots.ctypes.data_as(ctypes.c_void_p)), "fa_pool_append")
+        return slots[:n]
+
+    def release(self, seq: int):
+        _check(_lib.fa_pool_release(self._h, seq), "fa_pool_release")
+
+    def tables(self, seqs):
+        seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+        n = len(seqs)
+        table = np.zeros((max(n, 1), self.max_blocks_per_seq), np.int32)
+        lens = np.zeros(max(n, 1), np.int32)
+        _check(_lib.fa_pool_tables(self._h, seqs.ctypes.data_as(ctypes.c_void_p), n,
+                                   table.ctypes.data_as(ctypes.c_void_p), lens.ctypes.data_as(ctypes.c_void_p)),
+               "fa_pool_tables")
+        return table[:n], lens[:n]
+
+    def num_free(self) -> int:
+        return int(_lib.fa_pool_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(_lib.fa_pool_refcount(self._h, block))
+
+    def seq_len(self, seq: int) -> int:
+        return int(_lib.fa_pool_seq_len(self._h, seq))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.fa_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fa_copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """Copies cache block pairs[i, 0] onto pairs[i, 1] (pairs: int32 [n, 2] on the device)."""
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(pairs, "pairs", torch.int32, 2)
+    num_blocks, Hkv, _, d = k_cache.shape
+    _check(_lib.fa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], Hkv, d, num_blocks,
+                               _stream(stream)), "fa_copy_blocks")
 
 
 class DecodeGraph:
