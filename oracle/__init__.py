@@ -63,6 +63,11 @@ def _load():
         lib.ora_gather_kv.argtypes = [P, P, i, i, i, i, i, i, i, P]
         lib.ora_cache_append.argtypes = [P, P, P, i, i, i, i, i, P, P]
         lib.ora_rope_f64.argtypes = [P, P, P, i, l, i, P]
+        lib.ora_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.ora_e4m3_value.restype = d
+        lib.ora_quant_e4m3.argtypes = [P, l, ctypes.c_float, P]
+        lib.ora_cache_append_fp8.argtypes = [P, P, P, i, i, i, i, ctypes.c_float, ctypes.c_float, P, P]
+        lib.ora_paged_attention_fp8.argtypes = [P, P, P, d, d, P, P, P, i, i, i, i, i, i, i, d, P, l, P, P, i]
         lib.ora_rope_cache_append.argtypes = [P, P, P, P, P, i, P, i, i, i, i, i, i, P, P, P]
         lib.ora_paged_attention.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, i, d, P, P, i]
         lib.ora_paged_attention_rows.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, i, d,
@@ -227,6 +232,59 @@ def rope_cache_append(q, k, v, positions, cos_sin, slot_mapping, k_cache_bits: n
                                        Hq, Hkv, d, nb, bs, _ptr(qo), _ptr(kc), _ptr(vc))
     _check(st, "rope_cache_append")
     return qo, kc, vc
+
+
+# ---------------------------------------------------------- fp8 cache ----
+def e4m3_value(codes) -> np.ndarray:
+    """Values (float64) of E4M3 codes."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.ora_e4m3_value(int(c)) for c in codes.ravel()], dtype=np.float64).reshape(codes.shape)
+
+
+def quant_e4m3(x, scale: float) -> np.ndarray:
+    """E4M3 codes of float32(x) / float32(scale) (round to nearest even, saturating)."""
+    x = np.ascontiguousarray(x.numpy() if isinstance(x, torch.Tensor) else x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().ora_quant_e4m3(_ptr(x), x.size, float(scale), _ptr(out))
+    return out
+
+
+def cache_append_fp8(k, v, slot_mapping, k_cache: np.ndarray, v_cache: np.ndarray, k_scale: float, v_scale: float):
+    """Append into copies of the 8-bit caches (k [nb,Hkv,16,d], v [nb,Hkv,d,16]); returns them."""
+    kf = to_f64(k).astype(np.float32)
+    vf = to_f64(v).astype(np.float32)
+    N, Hkv, d = kf.shape
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8).copy()
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8).copy()
+    sm = _i32(slot_mapping)
+    st = _load().ora_cache_append_fp8(_ptr(kf), _ptr(vf), _ptr(sm), N, Hkv, d, kc.shape[0], float(k_scale),
+                                      float(v_scale), _ptr(kc), _ptr(vc))
+    _check(st, "cache_append_fp8")
+    return kc, vc
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, block_table, ctx_lens, q_lens,
+                        causal: bool, scale: float, rows=None, nthreads=None):
+    """Paged attention over the 8-bit caches -> (out f64 [rows or sum q, Hq, d], lse)."""
+    qb = to_bits(q)
+    total_q, Hq, d = qb.shape
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    nb, Hkv = kc.shape[0], kc.shape[1]
+    bt, cl, ql = _i32(block_table), _i32(ctx_lens), _i32(q_lens)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    n_out = total_q * Hq if r is None else len(r)
+    out = np.empty((n_out, d), np.float64)
+    lse = np.empty(n_out, np.float64)
+    st = _load().ora_paged_attention_fp8(_ptr(qb), _ptr(kc), _ptr(vc), float(k_scale), float(v_scale), _ptr(bt),
+                                         _ptr(cl), _ptr(ql), bt.shape[0], bt.shape[1], nb, Hq, Hkv, d, int(causal),
+                                         float(scale), _ptr(r), 0 if r is None else len(r), _ptr(out), _ptr(lse),
+                                         _threads(nthreads))
+    _check(st, "paged_attention_fp8")
+    if r is None:
+        return out.reshape(total_q, Hq, d), lse.reshape(total_q, Hq)
+    return out, lse
 
 
 def paged_attention(q, k_cache, v_cache, block_table, ctx_lens, q_lens, causal: bool, scale: float,

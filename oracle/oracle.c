@@ -527,11 +527,96 @@ int ora_rope_cache_append(const double* q, const double* k, const uint16_t* v, c
     return st;
 }
 
+/* --------------------------------------------------------- fp8 cache ---- */
+
+/*
+ * FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448).  Used for the 8-bit KV
+ * cache: the pages mention 8-bit matrix arithmetic ("8-bit MMA") without a
+ * scale convention; reading: one scale per cache (k_scale, v_scale), stored
+ * code = e4m3(x / scale) with the division in binary32 and round to nearest
+ * even, saturating at +-448; the value the code stands for is e4m3 * scale.
+ */
+double ora_e4m3_value(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);                 /* subnormal: m/8 * 2^(1-7) */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* nearest E4M3 code to y (exact comparison in double), ties to the even
+ * code, |y| beyond 448 saturates to +-448, NaN gives the NaN code */
+uint8_t ora_e4m3_rne(float y)
+{
+    if (y != y)
+        return 0x7F;
+    double a = fabs((double)y);
+    uint8_t best = 0;
+    double berr = a;                              /* code 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double err = fabs(ora_e4m3_value((uint8_t)c) - a);
+        if (err < berr || (err == berr && (c & 1) == 0 && (best & 1))) {
+            best = (uint8_t)c;
+            berr = err;
+        }
+    }
+    if (a > 448.0)
+        best = 0x7E;
+    return (uint8_t)(best | (y < 0 ? 0x80 : 0));
+}
+
+/* codes of x[i] / scale (x: binary32 values; division in binary32) */
+void ora_quant_e4m3(const float* x, long n, float scale, uint8_t* out)
+{
+    for (long i = 0; i < n; ++i) {
+        volatile float y = x[i] / scale;
+        out[i] = ora_e4m3_rne(y);
+    }
+}
+
+/*
+ * Append into the 8-bit cache.  k, v: binary32 values [N, Hkv, d] (bf16
+ * inputs decoded exactly).  K codes go to k_cache [num_blocks, Hkv, 16, d]
+ * like the bf16 append; V codes go to v_cache [num_blocks, Hkv, d, 16], the
+ * 16 tokens of a block contiguous for each channel (reading: the layout the
+ * decode kernel reads as token pairs).  slot < 0 skips the token.
+ */
+int ora_cache_append_fp8(const float* k, const float* v, const int32_t* slot_mapping, int N, int Hkv, int d,
+                         int num_blocks, float k_scale, float v_scale, uint8_t* k_cache, uint8_t* v_cache)
+{
+    for (int i = 0; i < N; ++i) {
+        long slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        if (slot >= (long)num_blocks * 16)
+            return ORA_ERR_BOUNDS;
+        long blk = slot / 16, off = slot % 16;
+        for (int h = 0; h < Hkv; ++h)
+            for (int c = 0; c < d; ++c) {
+                long src = ((long)i * Hkv + h) * d + c;
+                uint8_t kq, vq;
+                ora_quant_e4m3(k + src, 1, k_scale, &kq);
+                ora_quant_e4m3(v + src, 1, v_scale, &vq);
+                k_cache[((blk * Hkv + h) * 16 + off) * d + c] = kq;
+                v_cache[((blk * Hkv + h) * d + c) * 16 + off] = vq;
+            }
+    }
+    return ORA_OK;
+}
+
 /* ---------------------------------------------------- paged attention -- */
 
 typedef struct {
     work_queue wq;
     const uint16_t *q, *kc, *vc;
+    const uint8_t *kc8, *vc8;   /* 8-bit caches (when set, kc / vc are unused) */
+    double k_scale, v_scale;
     const int32_t *bt, *ctx_lens, *q_lens;
     const long* q_start;
     const int32_t* rows; /* NULL: every row; else (seq, qi, h) triples */
@@ -546,6 +631,19 @@ static int gather_seq_head(const paged_job* J, int s, int hk, uint16_t* tmp,
                            double* K, double* V)
 {
     const int ctx = J->ctx_lens[s], d = J->d;
+    if (J->kc8) {  /* 8-bit caches: follow the block table, decode, scale */
+        for (int t = 0; t < ctx; ++t) {
+            long phys = J->bt[(long)s * J->max_blocks + t / 16];
+            if (phys < 0 || phys >= J->num_blocks)
+                return ORA_ERR_BOUNDS;
+            long off = t % 16;
+            for (int c = 0; c < d; ++c) {
+                K[(long)t * d + c] = ora_e4m3_value(J->kc8[((phys * J->Hkv + hk) * 16 + off) * d + c]) * J->k_scale;
+                V[(long)t * d + c] = ora_e4m3_value(J->vc8[((phys * J->Hkv + hk) * d + c) * 16 + off]) * J->v_scale;
+            }
+        }
+        return ORA_OK;
+    }
     int st = ora_gather_kv(J->kc, J->bt, J->max_blocks, J->num_blocks, s, ctx, J->Hkv, d,
                            J->block_size, tmp);
     if (st)
@@ -645,6 +743,7 @@ done:
 }
 
 static int paged_common(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                        const uint8_t* k_cache8, const uint8_t* v_cache8, double k_scale, double v_scale,
                         const int32_t* block_table, const int32_t* ctx_lens,
                         const int32_t* q_lens, int num_seqs, int max_blocks_per_seq,
                         int num_blocks, int Hq, int Hkv, int d, int block_size, int causal,
@@ -670,6 +769,7 @@ static int paged_common(const uint16_t* q, const uint16_t* k_cache, const uint16
     pthread_mutex_init(&J.wq.lock, NULL);
     J.wq.total = rows ? nrows : (long)num_seqs * Hq;
     J.q = q; J.kc = k_cache; J.vc = v_cache; J.bt = block_table;
+    J.kc8 = k_cache8; J.vc8 = v_cache8; J.k_scale = k_scale; J.v_scale = v_scale;
     J.ctx_lens = ctx_lens; J.q_lens = q_lens; J.q_start = q_start; J.rows = rows;
     J.out = out; J.lse = lse; J.num_seqs = num_seqs; J.max_blocks = max_blocks_per_seq;
     J.num_blocks = num_blocks; J.Hq = Hq; J.Hkv = Hkv; J.d = d; J.block_size = block_size;
@@ -693,9 +793,25 @@ int ora_paged_attention(const uint16_t* q, const uint16_t* k_cache, const uint16
                         int num_blocks, int Hq, int Hkv, int d, int block_size, int causal,
                         double scale, double* out, double* lse, int nthreads)
 {
-    return paged_common(q, k_cache, v_cache, block_table, ctx_lens, q_lens, num_seqs,
+    return paged_common(q, k_cache, v_cache, NULL, NULL, 1.0, 1.0, block_table, ctx_lens, q_lens, num_seqs,
                         max_blocks_per_seq, num_blocks, Hq, Hkv, d, block_size, causal,
                         scale, NULL, 0, out, lse, nthreads);
+}
+
+/*
+ * Paged attention over the 8-bit caches (layouts and scales as in
+ * ora_cache_append_fp8): each cached key / value element is the E4M3 value
+ * of its code times k_scale / v_scale; the rest is ora_paged_attention.
+ */
+int ora_paged_attention_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache, double k_scale,
+                            double v_scale, const int32_t* block_table, const int32_t* ctx_lens,
+                            const int32_t* q_lens, int num_seqs, int max_blocks_per_seq, int num_blocks, int Hq,
+                            int Hkv, int d, int causal, double scale, const int32_t* rows, long nrows, double* out,
+                            double* lse, int nthreads)
+{
+    return paged_common(q, NULL, NULL, k_cache, v_cache, k_scale, v_scale, block_table, ctx_lens, q_lens,
+                        num_seqs, max_blocks_per_seq, num_blocks, Hq, Hkv, d, 16, causal, scale, rows, nrows,
+                        out, lse, nthreads);
 }
 
 /* Sampled rows: rows[3*r .. 3*r+2] = (seq, query index within the chunk, head). */
@@ -706,7 +822,7 @@ int ora_paged_attention_rows(const uint16_t* q, const uint16_t* k_cache,
                              int block_size, int causal, double scale, const int32_t* rows,
                              long nrows, double* out, double* lse, int nthreads)
 {
-    return paged_common(q, k_cache, v_cache, block_table, ctx_lens, q_lens, num_seqs,
+    return paged_common(q, k_cache, v_cache, NULL, NULL, 1.0, 1.0, block_table, ctx_lens, q_lens, num_seqs,
                         max_blocks_per_seq, num_blocks, Hq, Hkv, d, block_size, causal,
                         scale, rows, nrows, out, lse, nthreads);
 }

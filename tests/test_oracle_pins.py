@@ -445,3 +445,53 @@ def test_rope_rounds_once_from_fp64():
     assert qo[0, 0, 0] == 0x3F81           # 1.0078125
     assert qo[0, 0, 2] == _bits([2.0 ** -23])[0]
     assert qo[0, 0, 1] == _bits([0.5])[0] and qo[0, 0, 3] == _bits([0.25])[0]
+
+
+# ------------------------------------------------------- 8-bit cache -------
+# E4M3 codes are pinned to the format's definition (bias 7, 3 mantissa bits,
+# largest finite 448, S.1111.111 NaN); the 8-bit paged oracle is pinned to the
+# bf16 one on values both formats hold exactly.
+
+def test_e4m3_codes_from_the_format_definition():
+    cases = {0x00: 0.0, 0x38: 1.0, 0x30: 0.5, 0x7E: 448.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9,
+             0x08: 2.0 ** -6, 0x39: 1.125, 0x40: 2.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, val in cases.items():
+        assert oracle.e4m3_value([code])[0] == val, hex(code)
+    assert np.isnan(oracle.e4m3_value([0x7F, 0xFF])).all()
+
+
+def test_e4m3_every_code_round_trips():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF, 0x80)], np.uint8)
+    vals = oracle.e4m3_value(codes).astype(np.float32)
+    assert np.array_equal(oracle.quant_e4m3(vals, 1.0), codes)
+
+
+def test_e4m3_ties_to_even_and_saturation():
+    x = np.array([1.0625, 1.1875, 2.0 ** -10, 2.0 ** -10 * 1.01, 464.0, 1e6, -1e6, 0.0, -2.0 ** -12], np.float32)
+    assert list(oracle.quant_e4m3(x, 1.0)) == [0x38, 0x3A, 0x00, 0x01, 0x7E, 0x7E, 0xFE, 0x00, 0x80]
+    # the division by the scale happens in binary32 before rounding
+    assert oracle.quant_e4m3(np.array([3.0], np.float32), 1.5)[0] == 0x40
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.5, 4.0)])
+def test_fp8_paged_oracle_equals_bf16_on_representable_values(k_scale, v_scale):
+    p = W.paged_case(31, [40, 3, 130], [1, 2, 17], 4, 2, 64, num_blocks=64)
+    rng = np.random.default_rng(9)
+
+    def representable(shape, scale):
+        codes = oracle.quant_e4m3(rng.standard_normal(shape).astype(np.float32), 1.0)
+        return torch.from_numpy((oracle.e4m3_value(codes) * scale).astype(np.float32))
+
+    k_all = representable((64 * 16, 2, 64), k_scale)      # one value per pool slot
+    v_all = representable((64 * 16, 2, 64), v_scale)
+    slots = torch.arange(64 * 16, dtype=torch.int32)
+    z16 = np.zeros((64, 2, 16, 64), np.uint16)
+    kb, vb = oracle.cache_append(k_all, v_all, slots, z16, z16)
+    k8, v8 = oracle.cache_append_fp8(k_all, v_all, slots, np.zeros((64, 2, 16, 64), np.uint8),
+                                     np.zeros((64, 2, 64, 16), np.uint8), k_scale, v_scale)
+    assert np.array_equal(oracle.e4m3_value(k8) * k_scale, oracle.bits_to_f64(kb))
+    assert np.array_equal(oracle.e4m3_value(v8).transpose(0, 1, 3, 2) * v_scale, oracle.bits_to_f64(vb))
+    ref, lse_ref = oracle.paged_attention(p.q, kb, vb, p.block_table, p.ctx_lens, p.q_lens, True, p.scale)
+    got, lse = oracle.paged_attention_fp8(p.q, k8, v8, k_scale, v_scale, p.block_table, p.ctx_lens, p.q_lens, True,
+                                          p.scale)
+    assert np.array_equal(got, ref) and np.array_equal(lse, lse_ref)
