@@ -286,6 +286,32 @@ def bench_paged(F, timer, p, steps, warmup, ws, with_append=False):
     return dict(ms=ms, launches=launches, wall=wall)
 
 
+def bench_paged_fp8(F, timer, p, steps, warmup, ws, k_scale=0.0625, v_scale=0.03125):
+    """Decode over the 8-bit cache: the case's context and new tokens are
+    quantised into E4M3 caches first (outside the timed region)."""
+    nb, Hkv, _, d = p.k_cache.shape
+    kc = torch.zeros(nb, Hkv, 16, d, dtype=torch.uint8, device="cuda")
+    vc = torch.zeros(nb, Hkv, d, 16, dtype=torch.uint8, device="cuda")
+    used = np.unique(p.block_table.numpy()[p.block_table.numpy() >= 0])
+    slots = torch.from_numpy((used[:, None] * 16 + np.arange(16)[None, :]).ravel().astype(np.int32)).cuda()
+    ui = torch.from_numpy(used).long()
+    F.fa_cache_append_fp8(p.k_cache[ui].permute(0, 2, 1, 3).reshape(-1, Hkv, d).cuda(),
+                          p.v_cache[ui].permute(0, 2, 1, 3).reshape(-1, Hkv, d).cuda(), kc, vc, slots, k_scale, v_scale)
+    F.fa_cache_append_fp8(p.k_new.cuda(), p.v_new.cuda(), kc, vc, p.slot_mapping.cuda(), k_scale, v_scale)
+    q, bt, ctx, ql = p.q.cuda(), p.block_table.cuda(), p.ctx_lens.cuda(), p.q_lens.cuda()
+    out = torch.empty_like(q)
+    wsb = torch.empty(F.fa_paged_attn_workspace_size(p.num_seqs, p.max_blocks_per_seq, p.Hq, p.Hkv, p.d, p.total_q),
+                      dtype=torch.uint8, device="cuda")
+    mq = int(p.q_lens.max())
+
+    def step():
+        F.fa_paged_attn_fp8(q, kc, vc, k_scale, v_scale, bt, ctx, ql, causal=True, scale=p.scale, out=out,
+                            max_q_len=mq, ws=wsb)
+    ms, launches, wall, _ = timer.run(step, steps, warmup, ws)
+    kv = int(p.ctx_lens.numpy().astype(np.int64).sum()) * p.Hkv * p.d * 2
+    return dict(ms=reduce_max(ms, ws), launches=launches, wall=wall), kv
+
+
 def bench_decode_graph(F, p, warmup, n_steps=200):
     """Host submission cost of a decode step: n_steps steps issued back to
     back (no L2 flush: this measures launch overhead, not bandwidth), once as
@@ -553,6 +579,18 @@ def main():
                                  "traffic": None, "peak_source": f"{peak_src} hbm copy",
                                  "kernel": "rope_append_kernel<false>"}})
         del rq, rk, rv, rkc, rvc, rqo
+        # config 3 over the 8-bit (E4M3) cache: half the KV bytes
+        c3 = W.config3()
+        r8, kv8 = bench_paged_fp8(F, timer, c3, args.steps, args.warmup, ws)
+        gbs8 = kv8 / (r8["ms"] * 1e-3) / 1e9
+        sec.append({"workload": "config 3 over the 8-bit E4M3 cache (k_scale 1/16, v_scale 1/32): paged decode, 64 seqs "
+                                "ctx U[128,4096], Hq=12 Hkv=2 d=128",
+                    "metric": "paged-decode KV GB/s", "value": gbs8, "unit": "GB/s", "ms_per_step": r8["ms"],
+                    "kv_bytes": kv8, "gpu_launches": r8["launches"],
+                    "roofline": {"bound": "hbm", "achieved": gbs8, "peak": hbm, "unit": "GB/s", "frac": gbs8 / hbm,
+                                 "traffic": None, "peak_source": f"{peak_src} hbm copy",
+                                 "kernel": "paged_decode_kernel<128, true> + paged_merge_kernel<128>"}})
+        del c3
         # config 3 decode step (append of each sequence's new token + paged
         # attention), submitted back to back: eager calls vs one CUDA-graph replay
         sec.append(bench_decode_graph(F, W.config3(), args.warmup))

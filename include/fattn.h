@@ -148,6 +148,35 @@ fa_status fa_cache_append_rope(const void* q, const void* k, const void* v, cons
                                int d, int num_blocks, fa_dtype in_dtype, fa_stream_t stream);
 
 /*
+ * fa_cache_append_fp8 / fa_paged_attn_fp8 -- the 8-bit (E4M3) KV cache.
+ * Passage: "Further Reading" cites 8-bit matrix arithmetic ("8-bit MMA");
+ * the pages fix no format or scale convention.  Reading: E4M3 (1 sign, 4
+ * exponent bits, bias 7, 3 mantissa bits, largest finite 448, S.1111.111 NaN),
+ * one scale per cache: code = E4M3(x / scale), division in binary32, round to
+ * nearest even, saturating at +-448; the cached value is E4M3 * scale.
+ *   k_cache uint8 [num_blocks, Hkv, 16, d]   (a token's d codes contiguous)
+ *   v_cache uint8 [num_blocks, Hkv, d, 16]   (a channel's 16 tokens contiguous)
+ * fa_cache_append_fp8: k, v [N, Hkv, d] in `in_dtype`, slot_mapping as for
+ *   fa_cache_append; exact (bit-reproducible codes).  d = 128.
+ * fa_paged_attn_fp8: fa_paged_attn over these caches for decode rows only
+ *   ((Hq/Hkv) * max_q_len <= 16, else FA_ERR_UNSUPPORTED); the split-KV decode
+ *   kernel reads half the bytes of the bf16 cache, converts E4M3 to f16
+ *   (exactly) in registers, and computes in f16 MMAs with fp32 accumulation
+ *   (queries are converted bf16 -> f16: |q| must stay below 65504); k_scale
+ *   is folded into the score scale, v_scale multiplies the output.  Same
+ *   workspace as fa_paged_attn.  d = 128; scales finite and > 0.
+ */
+fa_status fa_cache_append_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                              const int32_t* slot_mapping, int N, int Hkv, int d, int num_blocks,
+                              float k_scale, float v_scale, fa_dtype in_dtype, fa_stream_t stream);
+fa_status fa_paged_attn_fp8(const void* q, const void* k_cache, const void* v_cache, float k_scale,
+                            float v_scale, const int32_t* block_table, const int32_t* ctx_lens,
+                            const int32_t* q_lens, void* out, int num_seqs, int max_blocks_per_seq,
+                            int num_blocks, int Hq, int Hkv, int d, int block_size, int causal,
+                            float scale, int total_q, int max_q_len, void* ws, size_t ws_bytes,
+                            fa_stream_t stream);
+
+/*
  * fa_paged_attn -- attention of packed queries against the paged cache.
  * Passage: "Paged Attention Kernels" (logical positions translated through
  * the block table; 16-token blocks); "FlashAttention-Style Kernels" (the

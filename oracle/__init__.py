@@ -66,6 +66,8 @@ def _load():
         lib.ora_e4m3_value.argtypes = [ctypes.c_uint8]
         lib.ora_e4m3_value.restype = d
         lib.ora_quant_e4m3.argtypes = [P, l, ctypes.c_float, P]
+        lib.ora_e4m3_rne_exhaustive.argtypes = [ctypes.c_float]
+        lib.ora_e4m3_rne_exhaustive.restype = ctypes.c_uint8
         lib.ora_cache_append_fp8.argtypes = [P, P, P, i, i, i, i, ctypes.c_float, ctypes.c_float, P, P]
         lib.ora_paged_attention_fp8.argtypes = [P, P, P, d, d, P, P, P, i, i, i, i, i, i, i, d, P, l, P, P, i]
         lib.ora_rope_cache_append.argtypes = [P, P, P, P, P, i, P, i, i, i, i, i, i, P, P, P]
@@ -248,6 +250,13 @@ def quant_e4m3(x, scale: float) -> np.ndarray:
     out = np.empty(x.shape, dtype=np.uint8)
     _load().ora_quant_e4m3(_ptr(x), x.size, float(scale), _ptr(out))
     return out
+
+
+def e4m3_rne_exhaustive(x) -> np.ndarray:
+    """E4M3 codes of float32 values by exhaustive nearest-code search (cross-check of quant_e4m3)."""
+    x = np.asarray(x, dtype=np.float32)
+    lib = _load()
+    return np.array([lib.ora_e4m3_rne_exhaustive(float(v)) for v in x.ravel()], np.uint8).reshape(x.shape)
 
 
 def cache_append_fp8(k, v, slot_mapping, k_cache: np.ndarray, v_cache: np.ndarray, k_scale: float, v_scale: float):

@@ -551,14 +551,40 @@ double ora_e4m3_value(uint8_t code)
 }
 
 /* nearest E4M3 code to y (exact comparison in double), ties to the even
- * code, |y| beyond 448 saturates to +-448, NaN gives the NaN code */
+ * code, |y| beyond 448 saturates to +-448, NaN gives the NaN code.  The
+ * positive codes 0 .. 0x7E increase with their value, so the two neighbours
+ * of |y| are found by bisection and the nearer one is kept. */
 uint8_t ora_e4m3_rne(float y)
 {
     if (y != y)
         return 0x7F;
     double a = fabs((double)y);
+    uint8_t best;
+    if (a >= 448.0) {
+        best = 0x7E;
+    } else {
+        int lo = 0, hi = 0x7E;                    /* value(lo) <= a < value(hi) */
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if (ora_e4m3_value((uint8_t)mid) <= a)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        double dl = a - ora_e4m3_value((uint8_t)lo), dh = ora_e4m3_value((uint8_t)hi) - a;
+        best = (uint8_t)(dl < dh ? lo : dh < dl ? hi : ((lo & 1) ? hi : lo));
+    }
+    return (uint8_t)(best | (y < 0 ? 0x80 : 0));
+}
+
+/* the same rounding by exhaustive search over all codes (test cross-check) */
+uint8_t ora_e4m3_rne_exhaustive(float y)
+{
+    if (y != y)
+        return 0x7F;
+    double a = fabs((double)y);
     uint8_t best = 0;
-    double berr = a;                              /* code 0 */
+    double berr = a;
     for (int c = 1; c <= 0x7E; ++c) {
         double err = fabs(ora_e4m3_value((uint8_t)c) - a);
         if (err < berr || (err == berr && (c & 1) == 0 && (best & 1))) {

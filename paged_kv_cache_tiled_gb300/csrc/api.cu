@@ -90,6 +90,12 @@ void set_launch_count(int n) { t_launches = n; }
 
 fa_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                               const uint64_t strides_bytes[3], const uint32_t box[4]) {
+    return encode_tmap_4d(map, base, dims, strides_bytes, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+fa_status encode_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                         const uint32_t box[4], CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_encode) {
@@ -106,9 +112,9 @@ fa_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t
     cuuint64_t gstr[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
     cuuint32_t bdim[4] = {box[0], box[1], box[2], box[3]};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gdim, gstr, bdim, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(map, dtype, 4, const_cast<void*>(base), gdim, gstr, bdim, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID_ARG;
 }
 

@@ -150,6 +150,53 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const void* __restrict
     }
 }
 
+// ------------------------------------------------------- 8-bit append -----
+// One thread quantises 16 channels of one (token, head) row of K and of V:
+// code = E4M3(x / scale) (binary32 division, round to nearest even,
+// saturating).  K codes are one 16-byte store into the row [blk][h][off];
+// V codes go to the channel-major block [blk][h][c][off], one byte per channel.
+template <bool kF32>
+__global__ void __launch_bounds__(256) cache_append_fp8_kernel(const void* __restrict__ k, const void* __restrict__ v,
+                                                               uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
+                                                               const int32_t* __restrict__ slots, int N, int Hkv, int d,
+                                                               int num_blocks, float k_scale, float v_scale,
+                                                               DevCtx ctx) {
+    const int cpr = d >> 4;  // 16-channel chunks per row
+    const long total = (long)N * Hkv * cpr;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int c = (int)(idx % cpr);
+        const long row = idx / cpr;
+        const int h = (int)(row % Hkv);
+        const long tok = row / Hkv;
+        const int slot = __ldg(slots + tok);
+        if (slot < 0) continue;
+        if (slot >= num_blocks * kBlock) {
+            raise_error(ctx, ERR_BOUNDS_BIT);
+            continue;
+        }
+        const long blk = slot / kBlock, off = slot % kBlock;
+        float x[16], y[16];
+        load8<kF32>(k, row * d + c * 16, *reinterpret_cast<float(*)[8]>(x));
+        load8<kF32>(k, row * d + c * 16 + 8, *reinterpret_cast<float(*)[8]>(x + 8));
+        load8<kF32>(v, row * d + c * 16, *reinterpret_cast<float(*)[8]>(y));
+        load8<kF32>(v, row * d + c * 16 + 8, *reinterpret_cast<float(*)[8]>(y + 8));
+        uint32_t kw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            kw[i] = f32x2_to_e4m3x2(__fdiv_rn(x[4 * i], k_scale), __fdiv_rn(x[4 * i + 1], k_scale)) |
+                    (f32x2_to_e4m3x2(__fdiv_rn(x[4 * i + 2], k_scale), __fdiv_rn(x[4 * i + 3], k_scale)) << 16);
+        *reinterpret_cast<uint4*>(kc + ((blk * Hkv + h) * kBlock + off) * d + c * 16) =
+            make_uint4(kw[0], kw[1], kw[2], kw[3]);
+        uint8_t* vrow = vc + ((blk * Hkv + h) * d + c * 16) * kBlock + off;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const uint32_t b = f32x2_to_e4m3x2(__fdiv_rn(y[i], v_scale), __fdiv_rn(y[i + 1], v_scale));
+            vrow[i * kBlock] = (uint8_t)(b & 0xFF);
+            vrow[(i + 1) * kBlock] = (uint8_t)(b >> 8);
+        }
+    }
+}
+
 // -------------------------------------------------------- block copy ------
 // Copy-on-write for the block pool: pair i copies physical block
 // pairs[2i] onto pairs[2i+1] in both caches (Hkv * 16 * d bf16 each),
@@ -364,6 +411,38 @@ fa_status fa_cache_append_rope(const void* q, const void* k, const void* v, cons
         rope_append_kernel<false><<<grid_for(work, 256), 256, 0, s>>>(
             q, k, v, positions, cos_sin, max_pos, static_cast<uint16_t*>(q_out), static_cast<uint16_t*>(k_cache),
             static_cast<uint16_t*>(v_cache), slot_mapping, N, Hq, Hkv, d, num_blocks, ctx);
+    st = cuda_status(cudaGetLastError());
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
+fa_status fa_cache_append_fp8(const void* k, const void* v, void* k_cache, void* v_cache, const int32_t* slot_mapping,
+                              int N, int Hkv, int d, int num_blocks, float k_scale, float v_scale, fa_dtype in_dtype,
+                              fa_stream_t stream) {
+    set_launch_count(0);
+    if (N < 0 || Hkv <= 0 || num_blocks < 0 || !(k_scale > 0.f) || !(k_scale < INFINITY) || !(v_scale > 0.f) ||
+        !(v_scale < INFINITY))
+        return FA_ERR_INVALID_ARG;
+    if (in_dtype != FA_BF16 && in_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (N == 0) return FA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) ||
+        !aligned16(v_cache))
+        return FA_ERR_INVALID_ARG;
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    const long work = (long)N * Hkv * (d / 16);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (in_dtype == FA_F32)
+        cache_append_fp8_kernel<true><<<grid_for(work, 256), 256, 0, s>>>(
+            k, v, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), slot_mapping, N, Hkv, d,
+            num_blocks, k_scale, v_scale, ctx);
+    else
+        cache_append_fp8_kernel<false><<<grid_for(work, 256), 256, 0, s>>>(
+            k, v, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), slot_mapping, N, Hkv, d,
+            num_blocks, k_scale, v_scale, ctx);
     st = cuda_status(cudaGetLastError());
     if (st == FA_OK) set_launch_count(1);
     return st;

@@ -28,6 +28,9 @@ void set_launch_count(int n);
 // cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
 fa_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                               const uint64_t strides_bytes[3], const uint32_t box[4]);
+// The same for any element type and swizzle mode.
+fa_status encode_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                         const uint32_t box[4], CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle);
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

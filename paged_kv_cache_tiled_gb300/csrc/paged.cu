@@ -147,12 +147,15 @@ __device__ long long cta_sum_ll(long long v, long long* red) {
     return t;
 }
 
-template <int D>
+// KV8: the 8-bit (E4M3) cache; its pages are half the bytes, so the ring is
+// twice as deep to keep the same bytes in flight.
+template <int D, bool KV8 = false>
 struct StreamSmem {
-    static constexpr int kPage = kBS * D * 2;  // bytes of one K (or V) page
-    static constexpr int kStage = 2 * kPage;   // K page + V page
-    static constexpr int kRing = kStreamWarps * kStreamStages * kStage;
-    static constexpr int kBars = kStreamWarps * kStreamStages + 1;
+    static constexpr int kPage = kBS * D * (KV8 ? 1 : 2);  // bytes of one K (or V) page
+    static constexpr int kStage = 2 * kPage;              // K page + V page
+    static constexpr int kStages = KV8 ? 2 * kStreamStages : kStreamStages;
+    static constexpr int kRing = kStreamWarps * kStages * kStage;
+    static constexpr int kBars = kStreamWarps * kStages + 1;
     static constexpr int kBytes = 1024 /*align slack*/ + kRing + kBars * 8 + 512;
 };
 
@@ -162,18 +165,29 @@ struct Cursor {
     int q0;                // first packed query row of sequence s
 };
 
-template <int D>
+// KV8 reads the 8-bit cache: K pages [16 tokens][D] bytes (128-byte swizzled
+// rows), V pages [D channels][16 tokens] bytes; the warp MMAs run in f16
+// (every E4M3 value is an f16 value; bf16 queries are converted to f16),
+// k_scale is folded into scale_log2 by the host and v_scale multiplies the
+// output.  The MMA's K dimension is taken in a permuted order so that one
+// ldmatrix lane word (4 consecutive bytes = 4 channels, or 4 tokens of V)
+// gives both B registers: logical k (2t, 2t+1, 2t+8, 2t+9) of a 16-wide step
+// = elements (4t .. 4t+3); queries are loaded in the same order for Q K^T,
+// and for P V the S tile's columns (tokens) are produced in that order by
+// loading K rows 4t+2nt+e into n-tile nt, column 2t+e.
+template <int D, bool KV8 = false>
 __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const uint16_t* __restrict__ q, const int32_t* __restrict__ bt,
                         const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ q_lens,
                         uint16_t* __restrict__ out, float* __restrict__ part_o, float2* __restrict__ part_ml,
                         int num_seqs, int mbps, int num_blocks, int Hq, int Hkv, int causal, float scale_log2,
-                        DevCtx ctx) {
+                        float v_scale, DevCtx ctx) {
     // the merge kernel that follows may be scheduled now; it waits for this
     // grid's completion before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    using L = StreamSmem<D>;
+    using L = StreamSmem<D, KV8>;
+    constexpr int kStreamStages = L::kStages;  // ring depth of this variant
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kRing);
@@ -310,10 +324,15 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
         uint8_t* kp = ring + stage * L::kStage;
         uint8_t* vp = kp + L::kPage;
         mbar_arrive_expect_tx(&wbar[stage], L::kStage);
+        if constexpr (KV8) {  // one box per page: K rows, V channel rows
+            tma_load_4d(kp, &tm_k, &wbar[stage], 0, 0, ci.hk, phys);
+            tma_load_4d(vp, &tm_v, &wbar[stage], 0, 0, ci.hk, phys);
+        } else {
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-            tma_load_4d(kp + h * 2048, &tm_k, &wbar[stage], h * 64, 0, ci.hk, phys);
-            tma_load_4d(vp + h * 2048, &tm_v, &wbar[stage], h * 64, 0, ci.hk, phys);
+            for (int h = 0; h < D / 64; ++h) {
+                tma_load_4d(kp + h * 2048, &tm_k, &wbar[stage], h * 64, 0, ci.hk, phys);
+                tma_load_4d(vp + h * 2048, &tm_v, &wbar[stage], h * 64, 0, ci.hk, phys);
+            }
         }
         advance(ci);
         if (i + 1 < n_pages) next_phys = __ldg(bt + (long)ci.s * mbps + ci.blk);
@@ -346,13 +365,27 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
 #pragma unroll
         for (int i = 0; i < 2; ++i)
             qrow[i] = rr[i] < nrows ? q + ((long)(cc.q0 + rr[i] / g) * Hq + cc.hk * g + rr[i] % g) * D : nullptr;
+        if constexpr (KV8) {
+            // f16, channels 4t .. 4t+3 of each 16-channel step (the permuted K order)
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const int c = ks * 16 + tig * 2;
-            qa[ks][0] = qrow[0] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[0] + c)) : 0u;
-            qa[ks][1] = qrow[1] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[1] + c)) : 0u;
-            qa[ks][2] = qrow[0] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[0] + c + 8)) : 0u;
-            qa[ks][3] = qrow[1] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[1] + c + 8)) : 0u;
+            for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint2 w = qrow[i] ? __ldg(reinterpret_cast<const uint2*>(qrow[i] + ks * 16 + tig * 4))
+                                            : make_uint2(0u, 0u);
+                    qa[ks][i] = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+                    qa[ks][i + 2] = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int c = ks * 16 + tig * 2;
+                qa[ks][0] = qrow[0] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[0] + c)) : 0u;
+                qa[ks][1] = qrow[1] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[1] + c)) : 0u;
+                qa[ks][2] = qrow[0] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[0] + c + 8)) : 0u;
+                qa[ks][3] = qrow[1] ? __ldg(reinterpret_cast<const uint32_t*>(qrow[1] + c + 8)) : 0u;
+            }
         }
         // keys <= pos(row) are visible
         pos_r0 = causal ? ctx_len - q_len + gid / g : ctx_len - 1;
@@ -377,7 +410,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
             for (int i = 0; i < 2; ++i) {
                 const int r = rr[i];
                 if (r >= nrows) continue;
-                const float inv = ls[i] > 0.f ? 1.f / ls[i] : 0.f;
+                const float inv = ls[i] > 0.f ? v_scale / ls[i] : 0.f;
                 uint16_t* dst = out + ((long)(cc.q0 + r / g) * Hq + cc.hk * g + r % g) * D;
 #pragma unroll
                 for (int n = 0; n < D / 8; ++n)
@@ -393,7 +426,8 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
                 float* dst = part_o + (slot * kDecodeRows + r) * D;
 #pragma unroll
                 for (int n = 0; n < D / 8; ++n)
-                    *reinterpret_cast<float2*>(dst + n * 8 + tig * 2) = make_float2(o[n][2 * i], o[n][2 * i + 1]);
+                    *reinterpret_cast<float2*>(dst + n * 8 + tig * 2) =
+                        make_float2(o[n][2 * i] * v_scale, o[n][2 * i + 1] * v_scale);
                 if (tig == 0) part_ml[slot * kDecodeRows + r] = make_float2(ml[i], ls[i]);
             }
         }
@@ -421,14 +455,32 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
 
         // S = Q K^T : 16 rows x 16 tokens
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if constexpr (KV8) {
+            // matrix mi: n-tile mi & 1, 16-byte chunk 2j + (mi >> 1); its row r8
+            // is token 4 (r8 / 2) + 2 (mi & 1) + r8 % 2 (the S column order P V uses)
+            const int tok = (r8 >> 1) * 4 + 2 * (mi & 1) + (r8 & 1);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const int tok = (mi >> 1) * 8 + r8;
-            const int chunk = ks * 2 + (mi & 1);
-            uint32_t b0r, b1r, b2r, b3r;
-            ldsm_x4(kbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0r, b1r, b2r, b3r);
-            mma_bf16_16816(sc[0], qa[ks], b0r, b1r);
-            mma_bf16_16816(sc[1], qa[ks], b2r, b3r);
+            for (int j = 0; j < D / 32; ++j) {
+                const int chunk = 2 * j + (mi >> 1);
+                uint32_t w[4], b[8];
+                ldsm_x4(kbase + tok * D + ((chunk ^ (tok & 7)) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) e4m3x4_to_f16x4(w[m], b[2 * m], b[2 * m + 1]);
+                mma_f16_16816(sc[0], qa[2 * j], b[0], b[1]);
+                mma_f16_16816(sc[1], qa[2 * j], b[2], b[3]);
+                mma_f16_16816(sc[0], qa[2 * j + 1], b[4], b[5]);
+                mma_f16_16816(sc[1], qa[2 * j + 1], b[6], b[7]);
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const int tok = (mi >> 1) * 8 + r8;
+                const int chunk = ks * 2 + (mi & 1);
+                uint32_t b0r, b1r, b2r, b3r;
+                ldsm_x4(kbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0r, b1r, b2r, b3r);
+                mma_bf16_16816(sc[0], qa[ks], b0r, b1r);
+                mma_bf16_16816(sc[1], qa[ks], b2r, b3r);
+            }
         }
         // mask + online softmax (base 2)
         float x[2][4];
@@ -436,7 +488,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int t = tok0 + nt * 8 + tig * 2 + (e & 1);
+                const int t = KV8 ? tok0 + tig * 4 + nt * 2 + (e & 1) : tok0 + nt * 8 + tig * 2 + (e & 1);
                 const int lim = (e < 2) ? pos_r0 : pos_r1;
                 x[nt][e] = (t <= lim && t < ctx_len) ? sc[nt][e] * scale_log2 : -INFINITY;
             }
@@ -470,25 +522,55 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
                 o[n][3] *= a1;
             }
         }
-        uint32_t pa[4] = {pack_bf16x2(pr[0][0], pr[0][1]), pack_bf16x2(pr[0][2], pr[0][3]),
-                          pack_bf16x2(pr[1][0], pr[1][1]), pack_bf16x2(pr[1][2], pr[1][3])};
+        uint32_t pa[4];
+        if constexpr (KV8) {
+            pa[0] = pack_f16x2(pr[0][0], pr[0][1]);
+            pa[1] = pack_f16x2(pr[0][2], pr[0][3]);
+            pa[2] = pack_f16x2(pr[1][0], pr[1][1]);
+            pa[3] = pack_f16x2(pr[1][2], pr[1][3]);
+        } else {
+            pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
+            pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
+            pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
+            pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+        }
         // O += P V : V rows past the context are zeroed so stale cache words
         // (possibly NaN) cannot reach the accumulator through a zero weight
         const int nvalid = ctx_len - tok0;  // >= 1
-        const uint32_t zlo = (tig * 2 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t zhi = (tig * 2 + 8 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 9 < nvalid ? 0xffff0000u : 0u);
+        if constexpr (KV8) {
+            // V page rows are channels (16 token bytes each); matrix mi of
+            // step q4 is n-tile 4 q4 + mi; a lane word holds tokens 4t .. 4t+3
+            const uint32_t zb = (tig * 4 < nvalid ? 0x000000ffu : 0u) | (tig * 4 + 1 < nvalid ? 0x0000ff00u : 0u) |
+                                (tig * 4 + 2 < nvalid ? 0x00ff0000u : 0u) | (tig * 4 + 3 < nvalid ? 0xff000000u : 0u);
 #pragma unroll
-        for (int dn = 0; dn < D / 16; ++dn) {
-            const int tok = (mi & 1) * 8 + r8;
-            const int chunk = dn * 2 + (mi >> 1);
-            uint32_t b0r, b1r, b2r, b3r;
-            ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0r, b1r, b2r, b3r);
-            b0r &= zlo;
-            b2r &= zlo;
-            b1r &= zhi;
-            b3r &= zhi;
-            mma_bf16_16816(o[2 * dn], pa, b0r, b1r);
-            mma_bf16_16816(o[2 * dn + 1], pa, b2r, b3r);
+            for (int q4 = 0; q4 < D / 32; ++q4) {
+                uint32_t w[4];
+                ldsm_x4(vbase + ((4 * q4 + mi) * 8 + r8) * 16, w[0], w[1], w[2], w[3]);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t b0r, b1r;
+                    e4m3x4_to_f16x4(w[m] & zb, b0r, b1r);
+                    mma_f16_16816(o[4 * q4 + m], pa, b0r, b1r);
+                }
+            }
+        } else {
+            const uint32_t zlo =
+                (tig * 2 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 1 < nvalid ? 0xffff0000u : 0u);
+            const uint32_t zhi =
+                (tig * 2 + 8 < nvalid ? 0x0000ffffu : 0u) | (tig * 2 + 9 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int dn = 0; dn < D / 16; ++dn) {
+                const int tok = (mi & 1) * 8 + r8;
+                const int chunk = dn * 2 + (mi >> 1);
+                uint32_t b0r, b1r, b2r, b3r;
+                ldsm_x4_t(vbase + (chunk >> 3) * 2048 + sw128_offset(tok, chunk & 7), b0r, b1r, b2r, b3r);
+                b0r &= zlo;
+                b2r &= zlo;
+                b1r &= zhi;
+                b3r &= zhi;
+                mma_bf16_16816(o[2 * dn], pa, b0r, b1r);
+                mma_bf16_16816(o[2 * dn + 1], pa, b2r, b3r);
+            }
         }
         __syncwarp();
         if (lane == 0 && issued < n_pages) issue(issued++);
@@ -722,33 +804,50 @@ __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restr
     }
 }
 
-template <int D>
+template <int D, bool KV8 = false>
 static fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* bt,
                                const int32_t* ctx_lens, const int32_t* q_lens, void* out, const PagedWs& w,
                                uint8_t* ws, int num_seqs, int mbps, int num_blocks, int Hq, int Hkv, int causal,
-                               float scale, cudaStream_t s, const DevCtx& ctx, int* launches) {
+                               float scale, cudaStream_t s, const DevCtx& ctx, int* launches, float k_scale = 1.f,
+                               float v_scale = 1.f) {
     CUtensorMap tk, tv;
-    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)kBS, (uint64_t)Hkv, (uint64_t)num_blocks};
-    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)kBS * D * 2, (uint64_t)Hkv * kBS * D * 2};
-    const uint32_t box[4] = {64, (uint32_t)kBS, 1, 1};
-    fa_status st = encode_tmap_bf16_4d(&tk, k_cache, dims, strides, box);
-    if (st != FA_OK) return st;
-    if ((st = encode_tmap_bf16_4d(&tv, v_cache, dims, strides, box)) != FA_OK) return st;
-    using L = StreamSmem<D>;
+    fa_status st;
+    if constexpr (KV8) {
+        // K [blocks][Hkv][16][D] bytes, rows of D bytes, 128-byte swizzle;
+        // V [blocks][Hkv][D][16] bytes, one 16-byte row per channel
+        const uint64_t kd[4] = {(uint64_t)D, (uint64_t)kBS, (uint64_t)Hkv, (uint64_t)num_blocks};
+        const uint64_t vd[4] = {(uint64_t)kBS, (uint64_t)D, (uint64_t)Hkv, (uint64_t)num_blocks};
+        const uint64_t ks[3] = {(uint64_t)D, (uint64_t)kBS * D, (uint64_t)Hkv * kBS * D};
+        const uint64_t vs[3] = {(uint64_t)kBS, (uint64_t)kBS * D, (uint64_t)Hkv * kBS * D};
+        const uint32_t kb[4] = {(uint32_t)D, (uint32_t)kBS, 1, 1};
+        const uint32_t vb[4] = {(uint32_t)kBS, (uint32_t)D, 1, 1};
+        st = encode_tmap_4d(&tk, k_cache, kd, ks, kb, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != FA_OK) return st;
+        st = encode_tmap_4d(&tv, v_cache, vd, vs, vb, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != FA_OK) return st;
+    } else {
+        const uint64_t dims[4] = {(uint64_t)D, (uint64_t)kBS, (uint64_t)Hkv, (uint64_t)num_blocks};
+        const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)kBS * D * 2, (uint64_t)Hkv * kBS * D * 2};
+        const uint32_t box[4] = {64, (uint32_t)kBS, 1, 1};
+        st = encode_tmap_bf16_4d(&tk, k_cache, dims, strides, box);
+        if (st != FA_OK) return st;
+        if ((st = encode_tmap_bf16_4d(&tv, v_cache, dims, strides, box)) != FA_OK) return st;
+    }
+    using L = StreamSmem<D, KV8>;
     static bool attr_done = false;  // benign race: setting the attribute twice is harmless
     if (!attr_done) {
-        if (cudaFuncSetAttribute(paged_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) !=
+        if (cudaFuncSetAttribute(paged_decode_kernel<D, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) !=
             cudaSuccess)
             return FA_ERR_CUDA;
         attr_done = true;
     }
     float* part_o = reinterpret_cast<float*>(ws + w.part_o);
     float2* part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
-    const float scale_log2 = scale * 1.4426950408889634f;
+    const float scale_log2 = scale * k_scale * 1.4426950408889634f;
     const int grid = std::min(sm_count(), kMaxStreamCtas);
-    paged_decode_kernel<D><<<grid, kStreamWarps * 32, L::kBytes, s>>>(
+    paged_decode_kernel<D, KV8><<<grid, kStreamWarps * 32, L::kBytes, s>>>(
         tk, tv, static_cast<const uint16_t*>(q), bt, ctx_lens, q_lens, static_cast<uint16_t*>(out), part_o, part_ml,
-        num_seqs, mbps, num_blocks, Hq, Hkv, causal, scale_log2, ctx);
+        num_seqs, mbps, num_blocks, Hq, Hkv, causal, scale_log2, v_scale, ctx);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     ++*launches;
     cudaLaunchConfig_t cfg = {};
@@ -831,6 +930,37 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
         if (st != FA_OK) return st;
         ++launches;
     }
+    set_launch_count(launches);
+    return FA_OK;
+}
+
+fa_status fa_paged_attn_fp8(const void* q, const void* k_cache, const void* v_cache, float k_scale, float v_scale,
+                            const int32_t* block_table, const int32_t* ctx_lens, const int32_t* q_lens, void* out,
+                            int num_seqs, int max_blocks_per_seq, int num_blocks, int Hq, int Hkv, int d,
+                            int block_size, int causal, float scale, int total_q, int max_q_len, void* ws,
+                            size_t ws_bytes, fa_stream_t stream) {
+    set_launch_count(0);
+    if (num_seqs < 0 || max_blocks_per_seq < 0 || num_blocks < 0 || Hq <= 0 || Hkv <= 0 || total_q < 0 ||
+        max_q_len < 0 || !(scale > 0.f) || !(scale < INFINITY) || !(k_scale > 0.f) || !(k_scale < INFINITY) ||
+        !(v_scale > 0.f) || !(v_scale < INFINITY))
+        return FA_ERR_INVALID_ARG;
+    if (block_size != kBS || d != 128 || Hq % Hkv != 0) return FA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || total_q == 0 || max_q_len == 0) return FA_OK;
+    if (!is_decode_row(max_q_len, Hq / Hkv)) return FA_ERR_UNSUPPORTED;  // decode rows only
+    if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !q_lens || !out) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned32(out)) return FA_ERR_INVALID_ARG;
+    if (num_blocks == 0 || max_blocks_per_seq == 0) return FA_ERR_INVALID_ARG;
+    const PagedWs w = paged_ws_layout(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q);
+    if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return FA_ERR_WORKSPACE;
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    DevCtx ctx;
+    if ((st = make_ctx(&ctx)) != FA_OK) return st;
+    int launches = 0;
+    st = launch_decode<128, true>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w,
+                                  static_cast<uint8_t*>(ws), num_seqs, max_blocks_per_seq, num_blocks, Hq, Hkv, causal,
+                                  scale, reinterpret_cast<cudaStream_t>(stream), ctx, &launches, k_scale, v_scale);
+    if (st != FA_OK) return st;
     set_launch_count(launches);
     return FA_OK;
 }

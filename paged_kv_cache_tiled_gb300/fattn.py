@@ -30,7 +30,7 @@ EXPORTS = [
     "fa_cache_append_rope", "fa_decode_graph_create", "fa_decode_graph_launch", "fa_decode_graph_kernel_count",
     "fa_decode_graph_destroy", "fa_pool_create", "fa_pool_destroy", "fa_pool_add_seq", "fa_pool_fork",
     "fa_pool_append", "fa_pool_release", "fa_pool_tables", "fa_pool_num_free", "fa_pool_refcount", "fa_pool_seq_len",
-    "fa_copy_blocks",
+    "fa_copy_blocks", "fa_cache_append_fp8", "fa_paged_attn_fp8",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
@@ -76,6 +76,9 @@ def _load() -> ctypes.CDLL:
         "fa_pool_refcount": (I, [P, I]),
         "fa_pool_seq_len": (I, [P, I]),
         "fa_copy_blocks": (I, [P, P, P, I, I, I, I, P]),
+        "fa_cache_append_fp8": (I, [P, P, P, P, P, I, I, I, I, ctypes.c_float, ctypes.c_float, I, P]),
+        "fa_paged_attn_fp8": (I, [P, P, P, ctypes.c_float, ctypes.c_float, P, P, P, P, I, I, I, I, I, I, I, I,
+                                  ctypes.c_float, I, I, P, ctypes.c_size_t, P]),
         "fa_debug_force_timeout": (None, [I]),
         "fa_paged_attn_noalloc": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P]),
         "fa_last_launch_count": (I, []),
@@ -334,6 +337,49 @@ class DecodeGraph:
             self.close()
         except Exception:
             pass
+
+
+def fa_cache_append_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale: float, v_scale: float, stream=None):
+    """E4M3 codes of k/v [N, Hkv, d] (bf16 or fp32) / scale into k_cache uint8 [nb, Hkv, 16, d] and
+    v_cache uint8 [nb, Hkv, d, 16] at slot_mapping[N]."""
+    if k.dtype not in (torch.bfloat16, torch.float32) or v.dtype != k.dtype:
+        raise ValueError("k, v must both be bf16 or both fp32")
+    _need(k, "k", k.dtype, 3)
+    _need(v, "v", k.dtype, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    N, Hkv, d = k.shape
+    dt = FA_F32 if k.dtype == torch.float32 else FA_BF16
+    _check(_lib.fa_cache_append_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), N, Hkv, d,
+                                    k_cache.shape[0], float(k_scale), float(v_scale), dt, _stream(stream)),
+           "fa_cache_append_fp8")
+
+
+def fa_paged_attn_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, block_table, ctx_lens, q_lens,
+                      causal: bool = True, scale: float | None = None, out=None, max_q_len: int | None = None,
+                      ws=None, stream=None):
+    """Decode rows of q [total_q, Hq, d] against the 8-bit caches."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    _need(q_lens, "q_lens", torch.int32, 1)
+    total_q, Hq, d = q.shape
+    num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
+    num_seqs, mbps = block_table.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    max_q_len = total_q if max_q_len is None else max_q_len
+    nbytes = fa_paged_attn_workspace_size(num_seqs, mbps, Hq, Hkv, d, total_q)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(_lib.fa_paged_attn_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale),
+                                  _ptr(block_table), _ptr(ctx_lens), _ptr(q_lens), _ptr(out), num_seqs, mbps,
+                                  num_blocks, Hq, Hkv, d, 16, int(causal), float(scale), total_q, int(max_q_len),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "fa_paged_attn_fp8")
+    return out
 
 
 def fa_paged_attn_workspace_size(num_seqs, max_blocks_per_seq, Hq, Hkv, d, total_q) -> int:

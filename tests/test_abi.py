@@ -91,6 +91,18 @@ def test_host_validation(fattn):
     assert lib.fa_decode_graph_launch(None, None) == fattn.FA_ERR_INVALID_ARG
     assert lib.fa_decode_graph_kernel_count(None) == 0
     lib.fa_decode_graph_destroy(None)
+    # 8-bit cache: head dim, scales, chunks too long for the decode kernel
+    assert lib.fa_cache_append_fp8(dummy, dummy, dummy, dummy, dummy, 4, 2, 64, 8, 1.0, 1.0, 0,
+                                   None) == fattn.FA_ERR_UNSUPPORTED
+    assert lib.fa_cache_append_fp8(dummy, dummy, dummy, dummy, dummy, 4, 2, 128, 8, 0.0, 1.0, 0,
+                                   None) == fattn.FA_ERR_INVALID_ARG
+    need8 = lib.fa_paged_attn_workspace_size(2, 4, 8, 2, 128, 8)
+    assert lib.fa_paged_attn_fp8(dummy, dummy, dummy, 1.0, 1.0, dummy, dummy, dummy, dummy, 2, 4, 8, 8, 2, 128, 16,
+                                 1, 0.1, 8, 5, dummy, need8, None) == fattn.FA_ERR_UNSUPPORTED   # 4 * 5 > 16 rows
+    assert lib.fa_paged_attn_fp8(dummy, dummy, dummy, 1.0, -1.0, dummy, dummy, dummy, dummy, 2, 4, 8, 8, 2, 128, 16,
+                                 1, 0.1, 2, 1, dummy, need8, None) == fattn.FA_ERR_INVALID_ARG
+    assert lib.fa_paged_attn_fp8(dummy, dummy, dummy, 1.0, 1.0, dummy, dummy, dummy, dummy, 2, 4, 8, 8, 2, 64, 16,
+                                 1, 0.1, 2, 1, dummy, need8, None) == fattn.FA_ERR_UNSUPPORTED
     # masked prefill workspace
     assert lib.fa_prefill_masked_workspace_size(16384) >= 128 * 128 + 128 * 4
     assert lib.fa_prefill_masked(dummy, dummy, dummy, dummy, dummy, 1, 300, 4, 2, 64, 0, 0.1, None, dummy, 10,

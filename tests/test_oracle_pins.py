@@ -466,6 +466,15 @@ def test_e4m3_every_code_round_trips():
     assert np.array_equal(oracle.quant_e4m3(vals, 1.0), codes)
 
 
+def test_e4m3_bisection_equals_exhaustive_search():
+    rng = np.random.default_rng(12)
+    mids = (oracle.e4m3_value(np.arange(0, 0x7E)) + oracle.e4m3_value(np.arange(1, 0x7F))) / 2
+    x = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(2000) * 1e-3, mids, -mids,
+                        np.nextafter(mids.astype(np.float32), np.float32(0)), [447.9, 448.1, 500.0, 1e30]])
+    x = x.astype(np.float32)
+    assert np.array_equal(oracle.quant_e4m3(x, 1.0), oracle.e4m3_rne_exhaustive(x))
+
+
 def test_e4m3_ties_to_even_and_saturation():
     x = np.array([1.0625, 1.1875, 2.0 ** -10, 2.0 ** -10 * 1.01, 464.0, 1e6, -1e6, 0.0, -2.0 ** -12], np.float32)
     assert list(oracle.quant_e4m3(x, 1.0)) == [0x38, 0x3A, 0x00, 0x01, 0x7E, 0x7E, 0xFE, 0x00, 0x80]
