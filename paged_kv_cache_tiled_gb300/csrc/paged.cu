@@ -589,21 +589,23 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
 
 // Merges the partials of segments cut by stream range boundaries: for row r,
 // m = max_p m_p, l = sum_p 2^(m_p - m) l_p, O = sum_p 2^(m_p - m) O_p / l (base
-// 2, O_p unnormalised).  One single-warp CTA per (sequence, kv head, row):
+// 2, O_p unnormalised).  One CTA per (sequence, kv head) with one warp per
+// output row (as many warps as the batch's longest decode chunk has rows):
 // lane j owns channels 4j..4j+3 and piece j's statistics.  The CTAs are small
 // enough to be resident beside the decode kernel's, so the programmatic
 // launch lets them compute their offsets while it runs; they read partials
 // only after griddepcontrol.wait.
-constexpr int kMergeThreads = 32;
+constexpr int kMergeMaxThreads = 32 * kDecodeRows;
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
+__global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
                                                                     const int32_t* __restrict__ q_lens,
                                                                     const float* __restrict__ part_o,
                                                                     const float2* __restrict__ part_ml,
                                                                     uint16_t* __restrict__ out, int num_seqs,
                                                                     int Hq, int Hkv, int mbps, int W) {
-    const int s = blockIdx.x, hk = blockIdx.y, r = blockIdx.z, g = Hq / Hkv;
-    const int lane = threadIdx.x;
+    // one warp per output row: warp w of CTA (s, hk) merges row w
+    const int s = blockIdx.x, hk = blockIdx.y, r = threadIdx.x >> 5, g = Hq / Hkv;
+    const int lane = threadIdx.x & 31;
     const int ql_s = __ldg(q_lens + s), cl_s = __ldg(ctx_lens + s);
     const bool mine = is_decode_row(ql_s, g) && ql_s <= cl_s && cl_s <= mbps * kBS && r < g * ql_s;
     if (!mine) {
@@ -808,8 +810,8 @@ template <int D, bool KV8 = false>
 static fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* bt,
                                const int32_t* ctx_lens, const int32_t* q_lens, void* out, const PagedWs& w,
                                uint8_t* ws, int num_seqs, int mbps, int num_blocks, int Hq, int Hkv, int causal,
-                               float scale, cudaStream_t s, const DevCtx& ctx, int* launches, float k_scale = 1.f,
-                               float v_scale = 1.f) {
+                               float scale, int merge_rows, cudaStream_t s, const DevCtx& ctx, int* launches,
+                               float k_scale = 1.f, float v_scale = 1.f) {
     CUtensorMap tk, tv;
     fa_status st;
     if constexpr (KV8) {
@@ -851,8 +853,8 @@ static fa_status launch_decode(const void* q, const void* k_cache, const void* v
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     ++*launches;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_seqs, Hkv, kDecodeRows);
-    cfg.blockDim = dim3(kMergeThreads);
+    cfg.gridDim = dim3(num_seqs, Hkv, 1);
+    cfg.blockDim = dim3(32 * merge_rows);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -902,10 +904,13 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
     const int g = Hq / Hkv;
     int launches = 0;
     if (g <= kDecodeRows) {
+        const int merge_rows = (int)std::min<long>(kDecodeRows, (long)g * max_q_len);
         st = d == 128 ? launch_decode<128>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
-                                           max_blocks_per_seq, num_blocks, Hq, Hkv, causal, scale, s, ctx, &launches)
+                                           max_blocks_per_seq, num_blocks, Hq, Hkv, causal, scale, merge_rows, s, ctx,
+                                           &launches)
                       : launch_decode<64>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
-                                          max_blocks_per_seq, num_blocks, Hq, Hkv, causal, scale, s, ctx, &launches);
+                                          max_blocks_per_seq, num_blocks, Hq, Hkv, causal, scale, merge_rows, s, ctx,
+                                          &launches);
         if (st != FA_OK) return st;
     }
     if (!is_decode_row(max_q_len, g)) {
@@ -959,7 +964,8 @@ fa_status fa_paged_attn_fp8(const void* q, const void* k_cache, const void* v_ca
     int launches = 0;
     st = launch_decode<128, true>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w,
                                   static_cast<uint8_t*>(ws), num_seqs, max_blocks_per_seq, num_blocks, Hq, Hkv, causal,
-                                  scale, reinterpret_cast<cudaStream_t>(stream), ctx, &launches, k_scale, v_scale);
+                                  scale, (Hq / Hkv) * max_q_len, reinterpret_cast<cudaStream_t>(stream), ctx,
+                                  &launches, k_scale, v_scale);
     if (st != FA_OK) return st;
     set_launch_count(launches);
     return FA_OK;
