@@ -38,6 +38,10 @@
 #include <algorithm>
 #include <cmath>
 
+#include <memory>
+#include <mutex>
+#include <vector>
+
 #include "host_common.cuh"
 
 namespace fa {
@@ -111,6 +115,30 @@ __device__ __forceinline__ int sel(const int (&a)[2], int s) { return s ? a[1] :
 __device__ __forceinline__ int unit_of(int i, int G) {
     const int c = blockIdx.x;
     return i * G + ((i & 1) ? (G - 1 - c) : c);
+}
+
+// An explicit unit-to-CTA assignment computed on the host (dense causal
+// prefill, where every unit's cost is known there): CTA c runs units
+// unit[start[c] .. start[c+1]).  Passed by value as a kernel parameter, so
+// it needs no device memory and a captured graph keeps it.  n == 0: use
+// unit_of.
+constexpr int kMaxSchedCtas = 160;
+constexpr int kMaxSchedUnits = 2048;
+struct TcSched {
+    int n;
+    uint16_t start[kMaxSchedCtas + 1];
+    uint16_t unit[kMaxSchedUnits];
+};
+
+// This CTA's i-th unit, or -1 after its last one.
+__device__ __forceinline__ int cta_unit(const TcSched& sc, int i, int G, int num_units) {
+    if (sc.n > 0) {
+        const int k = sc.start[blockIdx.x] + i;
+        return k < sc.start[blockIdx.x + 1] ? (int)sc.unit[k] : -1;
+    }
+    if (i * G >= num_units) return -1;
+    const int u = unit_of(i, G);
+    return u < num_units ? u : -1;
 }
 
 template <int MODE>
@@ -249,7 +277,8 @@ __device__ __noinline__ void store_zero_row(uint16_t* orow, float* lse) {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const TcParams p,
+                   const __grid_constant__ TcSched sched) {
     using C = TcCfg<D>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -319,9 +348,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int fill = 0, qcnt = 0;
         bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
         for (int i = 0; ok; ++i) {
-            if (i * G >= num_units) break;
-            const int u = unit_of(i, G);
-            if (u >= num_units) continue;
+            const int u = cta_unit(sched, i, G, num_units);
+            if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             if (!unit_active<MODE>(p, U)) continue;
             for (int s = 0; s < 2 && ok; ++s) {
@@ -464,9 +492,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
 
         for (int i = 0; ok; ++i) {
-            if (i * G >= num_units) break;
-            const int u = unit_of(i, G);
-            if (u >= num_units) continue;
+            const int u = cta_unit(sched, i, G, num_units);
+            if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             if (!unit_active<MODE>(p, U)) continue;
             for (int s = 0; s < 2; ++s)
@@ -551,9 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int sc = 0, oc = 0;
         bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
         for (int i = 0; ok; ++i) {
-            if (i * G >= num_units) break;
-            const int u = unit_of(i, G);
-            if (u >= num_units) continue;
+            const int u = cta_unit(sched, i, G, num_units);
+            if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             const bool valid = r < sel(U.nrows, s);
             const int row = sel(U.row0, s) + r;  // row within T (dense) or within the chunk (paged)
@@ -767,7 +793,7 @@ fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, cud
 // ------------------------------------------------------------ launchers ---
 template <int D, int MODE>
 static fa_status launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p,
-                           int grid, cudaStream_t s) {
+                           int grid, cudaStream_t s, const TcSched& sched) {
     static bool attr_done = false;  // setting the attribute twice is harmless
     if (!attr_done) {
         if (cudaFuncSetAttribute(attn_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -775,14 +801,105 @@ static fa_status launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const C
             return FA_ERR_CUDA;
         attr_done = true;
     }
-    attn_tc_kernel<D, MODE><<<grid, kTcThreads, TcCfg<D>::kSmem, s>>>(tq, tk, tv, p);
+    attn_tc_kernel<D, MODE><<<grid, kTcThreads, TcCfg<D>::kSmem, s>>>(tq, tk, tv, p, sched);
     return cuda_status(cudaGetLastError());
 }
 
 template <int MODE>
 static fa_status launch_tc_d(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const TcParams& p, int grid, cudaStream_t s) {
-    return d == 128 ? launch_tc<128, MODE>(tq, tk, tv, p, grid, s) : launch_tc<64, MODE>(tq, tk, tv, p, grid, s);
+                             const TcParams& p, int grid, cudaStream_t s, const TcSched* sched = nullptr) {
+    static const TcSched kNone = {};  // n == 0: the unit_of order
+    const TcSched& sc = sched ? *sched : kNone;
+    return d == 128 ? launch_tc<128, MODE>(tq, tk, tv, p, grid, s, sc) : launch_tc<64, MODE>(tq, tk, tv, p, grid, s, sc);
+}
+
+// Balanced unit-to-CTA assignment for dense causal prefill.  A unit's cost is
+// its KV tiles plus a fixed start/epilogue cost of about 1.4 tiles (measured);
+// units go longest first to the least loaded CTA, then single moves and swaps
+// off the most loaded CTA continue while they lower the maximum (at most 4000
+// steps, stopping within 0.5 % of the mean load).
+// Cached per (B, T, Hq, Hkv, grid): the result depends on nothing else.
+static const TcSched* dense_schedule(const TcParams& p, int grid) {
+    if (!p.causal || p.num_units > kMaxSchedUnits || grid > kMaxSchedCtas || grid <= 0) return nullptr;
+    struct Key {
+        int B, T, Hq, Hkv, grid;
+        bool operator==(const Key& o) const {
+            return B == o.B && T == o.T && Hq == o.Hq && Hkv == o.Hkv && grid == o.grid;
+        }
+    };
+    static std::mutex mu;
+    static std::vector<std::pair<Key, std::unique_ptr<TcSched>>> cache;
+    const Key key{p.B, p.T, p.Hq, p.Hkv, grid};
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto& e : cache)
+        if (e.first == key) return e.second.get();
+    // unit costs, in the unit numbering decode_unit uses (rank-major, longest first)
+    const int nqt = (p.T + kTcRows - 1) / kTcRows, n = p.num_units;
+    std::vector<double> cost(n);
+    for (int u = 0; u < n; ++u) {
+        int kt;
+        if (p.pair_heads) {
+            const int upt = p.B * p.Hkv * (p.g / 2);
+            kt = nqt - u / upt;  // query tile nqt - 1 - rank sees qt + 1 KV tiles
+        } else {
+            const int upt = p.B * p.Hq, ntp = (nqt + 1) / 2;
+            kt = std::min(nqt, 2 * (ntp - 1 - u / upt) + 2);
+        }
+        cost[u] = kt + 1.4;
+    }
+    std::vector<std::vector<int>> bins(grid);
+    std::vector<double> load(grid, 0.0);
+    for (int u = 0; u < n; ++u) {  // u already runs longest first
+        const int b = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+        bins[b].push_back(u);
+        load[b] += cost[u];
+    }
+    double mean = 0.0;
+    for (double x : load) mean += x;
+    mean /= grid;
+    for (int iter = 0; iter < 4000; ++iter) {
+        const int a = (int)(std::max_element(load.begin(), load.end()) - load.begin());
+        if (load[a] <= mean * 1.005) break;  // within 0.5 % of the ideal
+        bool moved = false;
+        for (int b = 0; b < grid && !moved; ++b) {
+            if (b == a) continue;
+            for (size_t i = 0; i < bins[a].size() && !moved; ++i) {
+                const int x = bins[a][i];
+                if (load[b] + cost[x] < load[a] - 1e-9) {
+                    bins[b].push_back(x);
+                    bins[a].erase(bins[a].begin() + i);
+                    load[b] += cost[x];
+                    load[a] -= cost[x];
+                    moved = true;
+                    break;
+                }
+                for (size_t j = 0; j < bins[b].size(); ++j) {
+                    const int y = bins[b][j];
+                    const double na = load[a] - cost[x] + cost[y], nb = load[b] - cost[y] + cost[x];
+                    if (cost[y] < cost[x] && na < load[a] - 1e-9 && nb < load[a] - 1e-9) {
+                        bins[a][i] = y;
+                        bins[b][j] = x;
+                        load[a] = na;
+                        load[b] = nb;
+                        moved = true;
+                        break;
+                    }
+                }
+            }
+        }
+        if (!moved) break;
+    }
+    auto sc = std::make_unique<TcSched>();
+    sc->n = n;
+    int k = 0;
+    for (int c = 0; c < grid; ++c) {
+        std::sort(bins[c].begin(), bins[c].end());  // longest first within the CTA
+        sc->start[c] = (uint16_t)k;
+        for (int u : bins[c]) sc->unit[k++] = (uint16_t)u;
+    }
+    sc->start[grid] = (uint16_t)k;
+    cache.emplace_back(key, std::move(sc));
+    return cache.back().second.get();
 }
 
 static fa_status dense_maps(const void* q, const void* k, const void* v, int B, int T, int Hq, int Hkv, int d,
@@ -878,7 +995,8 @@ fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int
     TcParams p = base_params(B, T, Hq, Hkv, causal, scale, out, lse, ctx);
     p.num_units = dense_units(p);
     const int grid = std::min(p.num_units, sm_count());
-    st = launch_tc_d<MODE_DENSE>(d, tq, tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    st = launch_tc_d<MODE_DENSE>(d, tq, tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream),
+                                 dense_schedule(p, grid));
     if (st == FA_OK) set_launch_count(1);
     return st;
 }
