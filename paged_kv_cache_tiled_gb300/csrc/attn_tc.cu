@@ -612,25 +612,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // scale.  Decided per warp (the general path also covers plain rows),
                 // because the general path issues warp-collective TMEM stores.
                 const bool plain = !__any_sync(0xffffffffu, !((cls == 1) && (lim >= kTcRows)));
-                // pass 1: row max, 64 columns per TMEM wait.  In the general case
-                // the masked, scaled logits are written back over S so that pass
-                // 2 reads them instead of re-reading the mask.
+                // pass 1: row max.  A plain tile loads its whole 128-column score row
+                // with one TMEM wait; otherwise 64 columns per wait, and the masked,
+                // scaled logits are written back over S so that pass 2 reads them
+                // instead of re-reading the mask.
                 // 8 independent partial maxima / sums keep the reductions off a
                 // single serial dependency chain
                 float mxp[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
-                const bool vec_mask = mrow && ((p.T & 3) == 0);
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t raw[64];
-                    tmem_ld32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
-                    tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
-                    tmem_wait_ld();
-                    if (plain) {  // scale > 0: the max of the raw scores gives the max of the scaled ones
+                if (plain) {  // scale > 0: the max of the raw scores gives the max of the scaled ones
+                    uint32_t raw[kTcRows];
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) mxp[j & 7] = fmaxf(mxp[j & 7], __uint_as_float(raw[j]));
-                    } else {
+                    for (int c = 0; c < kTcRows / 32; ++c)
+                        tmem_ld32(trow + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < kTcRows; ++j) mxp[j & 7] = fmaxf(mxp[j & 7], __uint_as_float(raw[j]));
+                } else {
+                    const bool vec_mask = mrow && ((p.T & 3) == 0);
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t raw[64];
+                        tmem_ld32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+                        tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+                        tmem_wait_ld();
 #pragma unroll
                         for (int j4 = 0; j4 < 16; ++j4) {
                             float mv[4] = {0.f, 0.f, 0.f, 0.f};
@@ -655,11 +661,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tmem_st32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
                         tmem_st32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     }
+                    tmem_wait_st();
                 }
                 float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                  fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
                 if (plain) mx *= p.scale_log2;
-                else tmem_wait_st();
                 const float m_new = fmaxf(m, mx);
                 const bool need = m_new > m + kRescaleThreshold;
                 float alpha = 1.f;
@@ -675,8 +681,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const bool rescale_o = warp_rescale && it > 0;
                 // pass 2: P = 2^(logit - m) as bf16.  Half h reads S columns
                 // [64h, 64h+64) and writes P columns [32h, 32h+32), only over S
-                // columns already read.
+                // columns already read; without a rescale each half goes to the MMA
+                // warp as soon as it is stored, so P*V over keys 0..63 overlaps half 1.
                 float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                const float sc2 = plain ? p.scale_log2 : 1.f;  // logits already scaled in the general case
+                const float neg_m = -m_use;
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     uint32_t raw[64];
@@ -684,8 +693,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     tmem_wait_ld();
                     uint32_t pk[32];
-                    const float sc2 = plain ? p.scale_log2 : 1.f;  // logits already scaled in the general case
-                    const float neg_m = -m_use;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float p0 = fast_exp2(fmaf(__uint_as_float(raw[2 * j]), sc2, neg_m));
@@ -694,12 +701,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         pk[j] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(trow + s_col + h * 32, pk);
-                }
-                if (!rescale_o) {  // P complete: hand the tile to the MMA warp
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(&pfull[2 * s]);
-                    mbar_arrive(&pfull[2 * s + 1]);
+                    if (!rescale_o) {
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(&pfull[2 * s + h]);
+                    }
                 }
                 l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
                 if (rescale_o) {
