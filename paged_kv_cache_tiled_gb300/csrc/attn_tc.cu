@@ -628,7 +628,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tmem_ld32(trow + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < kTcRows; ++j) mxp[j & 7] = fmaxf(mxp[j & 7], __uint_as_float(raw[j]));
+                    for (int j = 0; j < kTcRows; j += 2)
+                        mxp[(j >> 1) & 7] = fmax3f(mxp[(j >> 1) & 7], __uint_as_float(raw[j]), __uint_as_float(raw[j + 1]));
                 } else {
                     const bool vec_mask = mrow && ((p.T & 3) == 0);
 #pragma unroll 1
@@ -683,9 +684,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // [64h, 64h+64) and writes P columns [32h, 32h+32), only over S
                 // columns already read; without a rescale each half goes to the MMA
                 // warp as soon as it is stored, so P*V over keys 0..63 overlaps half 1.
-                float rsp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                const float sc2 = plain ? p.scale_log2 : 1.f;  // logits already scaled in the general case
-                const float neg_m = -m_use;
+                // column pairs go through packed f32x2 FMA / add (one instruction per pair)
+                float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                const float sc = plain ? p.scale_log2 : 1.f;  // logits already scaled in the general case
+                const float2 sc2 = make_float2(sc, sc), neg_m = make_float2(-m_use, -m_use);
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     uint32_t raw[64];
@@ -695,10 +698,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint32_t pk[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(raw[2 * j]), sc2, neg_m));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(raw[2 * j + 1]), sc2, neg_m));
-                        rsp[j & 7] += p0 + p1;
-                        pk[j] = pack_bf16x2(p0, p1);
+                        const float2 x =
+                            __ffma2_rn(make_float2(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), sc2, neg_m);
+                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        rsp[j & 3] = __fadd2_rn(rsp[j & 3], pp);
+                        pk[j] = pack_bf16x2(pp.x, pp.y);
                     }
                     tmem_st32(trow + s_col + h * 32, pk);
                     if (!rescale_o) {
@@ -707,7 +711,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mbar_arrive(&pfull[2 * s + h]);
                     }
                 }
-                l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
+                l += ((rsp[0].x + rsp[0].y) + (rsp[1].x + rsp[1].y)) + ((rsp[2].x + rsp[2].y) + (rsp[3].x + rsp[3].y));
                 if (rescale_o) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
