@@ -608,28 +608,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int lim = vis_end - kv0;  // visible columns of this tile: [0, lim)
                 const int cls = tile_class<MODE>(p, U, s, kt);
                 const float* mrow = (cls == 2 && valid) ? p.mask + (long)row * p.T + kv0 : nullptr;
-                // every column visible and no mask values to add: scores only need the
-                // scale.  Decided per warp (the general path also covers plain rows),
-                // because the general path issues warp-collective TMEM stores.
-                const bool plain = !__any_sync(0xffffffffu, !((cls == 1) && (lim >= kTcRows)));
-                // pass 1: row max.  A plain tile loads its whole 128-column score row
-                // with one TMEM wait; otherwise 64 columns per wait, and the masked,
-                // scaled logits are written back over S so that pass 2 reads them
-                // instead of re-reading the mask.
-                // 8 independent partial maxima / sums keep the reductions off a
-                // single serial dependency chain
+                // cls is the same for the whole warp (it depends on the slot and the
+                // tile only).  Without mask values (cls 0 or 1) the scores need only
+                // the scale and the column limit, both applied in registers; with
+                // mask values (cls 2, "general") the masked, scaled logits are
+                // written back over S in pass 1 so that pass 2 reads them instead of
+                // re-reading the mask.
+                const bool general = cls == 2;
+                const int vlim = cls == 0 ? 0 : lim;  // visible columns of this row: [0, vlim)
+                // every column of every row of the warp visible and no mask values
+                const bool plain = !general && __all_sync(0xffffffffu, vlim >= kTcRows);
+                // pass 1: row max.  Without mask values the whole 128-column score row
+                // is loaded with one TMEM wait; the general case takes 64 columns per
+                // wait.  8 independent partial maxima / sums keep the reductions off a
+                // single serial dependency chain.
                 float mxp[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
-                if (plain) {  // scale > 0: the max of the raw scores gives the max of the scaled ones
+                if (!general) {  // scale > 0: the max of the raw scores gives the max of the scaled ones
                     uint32_t raw[kTcRows];
 #pragma unroll
                     for (int c = 0; c < kTcRows / 32; ++c)
                         tmem_ld32(trow + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * c));
                     tmem_wait_ld();
+                    if (plain) {
 #pragma unroll
-                    for (int j = 0; j < kTcRows; j += 2)
-                        mxp[(j >> 1) & 7] = fmax3f(mxp[(j >> 1) & 7], __uint_as_float(raw[j]), __uint_as_float(raw[j + 1]));
+                        for (int j = 0; j < kTcRows; j += 2)
+                            mxp[(j >> 1) & 7] =
+                                fmax3f(mxp[(j >> 1) & 7], __uint_as_float(raw[j]), __uint_as_float(raw[j + 1]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kTcRows; j += 2)
+                            mxp[(j >> 1) & 7] = fmax3f(mxp[(j >> 1) & 7], j < vlim ? __uint_as_float(raw[j]) : -INFINITY,
+                                                       j + 1 < vlim ? __uint_as_float(raw[j + 1]) : -INFINITY);
+                    }
                 } else {
                     const bool vec_mask = mrow && ((p.T & 3) == 0);
 #pragma unroll 1
@@ -652,7 +664,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int j = j0 + e;
-                                const float x = (cls == 0 || j >= lim)
+                                const float x = j >= lim
                                                     ? -INFINITY
                                                     : fmaf(__uint_as_float(raw[4 * j4 + e]), p.scale_log2, mv[e] * kLog2e);
                                 raw[4 * j4 + e] = __float_as_uint(x);
@@ -666,7 +678,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                  fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-                if (plain) mx *= p.scale_log2;
+                if (!general) mx *= p.scale_log2;
                 const float m_new = fmaxf(m, mx);
                 const bool need = m_new > m + kRescaleThreshold;
                 float alpha = 1.f;
@@ -687,7 +699,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // column pairs go through packed f32x2 FMA / add (one instruction per pair)
                 float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
-                const float sc = plain ? p.scale_log2 : 1.f;  // logits already scaled in the general case
+                const float sc = general ? 1.f : p.scale_log2;  // logits already scaled in the general case
                 const float2 sc2 = make_float2(sc, sc), neg_m = make_float2(-m_use, -m_use);
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
@@ -696,13 +708,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
                     tmem_wait_ld();
                     uint32_t pk[32];
+                    if (plain || general) {  // every column visible, or masked logits already -inf
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float2 x =
-                            __ffma2_rn(make_float2(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), sc2, neg_m);
-                        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                        rsp[j & 3] = __fadd2_rn(rsp[j & 3], pp);
-                        pk[j] = pack_bf16x2(pp.x, pp.y);
+                        for (int j = 0; j < 32; ++j) {
+                            const float2 x = __ffma2_rn(
+                                make_float2(__uint_as_float(raw[2 * j]), __uint_as_float(raw[2 * j + 1])), sc2, neg_m);
+                            const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                            rsp[j & 3] = __fadd2_rn(rsp[j & 3], pp);
+                            pk[j] = pack_bf16x2(pp.x, pp.y);
+                        }
+                    } else {
+                        // columns at or past the row's limit get probability 0.  The
+                        // logit takes the general case's operations (scaled with a zero
+                        // addend, then the max subtracted), so that a causal limit and
+                        // an additive -inf mask of the same shape give bit-identical
+                        // results.
+                        const int c0 = h * 64;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float2 x = __ffma2_rn(make_float2(fmaf(__uint_as_float(raw[2 * j]), p.scale_log2, 0.f),
+                                                                    fmaf(__uint_as_float(raw[2 * j + 1]), p.scale_log2, 0.f)),
+                                                        make_float2(1.f, 1.f), neg_m);
+                            const float2 pp = make_float2(c0 + 2 * j < vlim ? fast_exp2(x.x) : 0.f,
+                                                          c0 + 2 * j + 1 < vlim ? fast_exp2(x.y) : 0.f);
+                            rsp[j & 3] = __fadd2_rn(rsp[j & 3], pp);
+                            pk[j] = pack_bf16x2(pp.x, pp.y);
+                        }
                     }
                     tmem_st32(trow + s_col + h * 32, pk);
                     if (!rescale_o) {
