@@ -532,15 +532,16 @@ def main():
         c4 = W.config4()
         r4 = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks, masked=True)
         r4c = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks, causal=True)
-        for r, name in ((r4, "additive mask M (-inf above diagonal) via fa_prefill_masked"),
-                        (r4c, "causal flag via fa_prefill")):
+        for r, name, tkey in ((r4, "additive mask M (-inf above diagonal) via fa_prefill_masked", None),
+                              (r4c, "causal flag via fa_prefill", "attn_tc_dense_c4")):
             sec.append({"workload": f"config 4: long prefill B=1 T=16384 Hq=32 Hkv=8 d=128, {name}",
                         "metric": "prefill attn TFLOP/s", "value": r["tflops"], "unit": "TFLOP/s",
                         "ms_per_step": r["ms"], "gpu_launches": r["launches"],
                         "roofline": {"bound": "tensor", "achieved": r["tflops"],
                                      "peak": float(peaks.get("bf16_tflops_sustained", tc_peak)), "unit": "TFLOP/s",
                                      "frac": r["tflops"] / float(peaks.get("bf16_tflops_sustained", tc_peak)),
-                                     "traffic": None, "peak_source": f"{peak_src} bf16 sustained"}})
+                                     "traffic": traffic.get(tkey) if tkey else None,
+                                     "peak_source": f"{peak_src} bf16 sustained"}})
         del c4, r4, r4c
         torch.cuda.empty_cache()
         # config 5: append + chunked prefill over the paged cache
