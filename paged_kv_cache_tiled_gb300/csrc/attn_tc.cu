@@ -478,14 +478,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         (acc_first || kk > 0));
             }
         };
-        // waits for each half of P_s in turn and issues its P*V MMAs
+        // waits for P_s and issues its P*V MMAs.  The second half is signalled
+        // after the first, so one wait covers both.
         auto pv = [&](int s, int vidx, bool acc_first) -> bool {
-            for (int h = 0; h < 2; ++h) {
-                if (!mbar_wait_warp(&pfull[2 * s + h], (s ? pc1 : pc0) & 1, lim_ns, abort_flag)) return false;
-                tc_fence_after();
-                if (lane == 0) issue_pv_half(s, vidx, h, acc_first);
-                __syncwarp();
+            if (!mbar_wait_warp(&pfull[2 * s + 1], (s ? pc1 : pc0) & 1, lim_ns, abort_flag)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                issue_pv_half(s, vidx, 0, acc_first);
+                issue_pv_half(s, vidx, 1, acc_first);
             }
+            __syncwarp();
             if (s) ++pc1;
             else ++pc0;
             return true;
