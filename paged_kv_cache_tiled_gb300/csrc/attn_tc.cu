@@ -432,8 +432,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int cons = 0, ucnt = 0, pc0 = 0, pc1 = 0;  // pc: P tiles consumed per slot
         bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
 
-        auto wait_v = [&](int vidx, int vkt, int kv_len) -> bool {
-            if (!mbar_wait_warp(&full[vidx % S], (vidx / S) & 1, lim_ns, abort_flag)) return false;
+        // `ready`: the phase was already seen complete by every lane (mbar_test3)
+        auto wait_v = [&](int vidx, int vkt, int kv_len, bool ready = false) -> bool {
+            if (!ready && !mbar_wait_warp(&full[vidx % S], (vidx / S) & 1, lim_ns, abort_flag)) return false;
             if constexpr (MODE == MODE_PAGED) {
                 // Rows past the context inside the last partly filled block
                 // may hold stale words; zero them so a zero probability never
@@ -480,8 +481,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         // waits for P_s and issues its P*V MMAs.  The second half is signalled
         // after the first, so one wait covers both.
-        auto pv = [&](int s, int vidx, bool acc_first) -> bool {
-            if (!mbar_wait_warp(&pfull[2 * s + 1], (s ? pc1 : pc0) & 1, lim_ns, abort_flag)) return false;
+        auto pv = [&](int s, int vidx, bool acc_first, bool ready = false) -> bool {
+            if (!ready && !mbar_wait_warp(&pfull[2 * s + 1], (s ? pc1 : pc0) & 1, lim_ns, abort_flag)) return false;
             tc_fence_after();
             if (lane == 0) {
                 issue_pv_half(s, vidx, 0, acc_first);
@@ -506,21 +507,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int kt = U.kt0; kt < U.n_kt && ok; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
                 const int kidx = cons + 2 * it;
+                // Before slot 0's MMAs the previous V tile, P_0 and this K tile are
+                // probed together: each barrier check in this warp costs the tensor
+                // pipe idle time, and three probes in flight cost about one.
+                // (Paged K tiles arrive box by box and are rarely complete this
+                // early, so paged mode waits as before.)
+                bool v_rdy = false, p0_rdy = false, k_rdy = false;
+                if (MODE != MODE_PAGED && it > 0) {
+                    uint32_t r[3];
+                    mbar_test3(&full[prev_v % S], (prev_v / S) & 1, &pfull[1], pc0 & 1, &full[kidx % S],
+                               (kidx / S) & 1, r);
+                    v_rdy = __all_sync(0xffffffffu, r[0]);
+                    p0_rdy = __all_sync(0xffffffffu, r[1]);
+                    k_rdy = __all_sync(0xffffffffu, r[2]);
+                }
                 for (int s = 0; s < 2 && ok; ++s) {
                     // P_s V of the previous tile goes out as soon as P_s is
                     // ready; only the Q K^T after it waits for this tile's K
                     if (it > 0) {
-                        if (s == 0 && !wait_v(prev_v, prev_kt, U.kv_len)) {
+                        if (s == 0 && !wait_v(prev_v, prev_kt, U.kv_len, v_rdy)) {
                             ok = false;
                             break;
                         }
-                        if (!pv(s, prev_v, it > 1)) {
+                        if (!pv(s, prev_v, it > 1, s == 0 && p0_rdy)) {
                             ok = false;
                             break;
                         }
                     }
                     if (s == 0) {
-                        if (!mbar_wait_warp(&full[kidx % S], (kidx / S) & 1, lim_ns, abort_flag)) {
+                        if (!k_rdy && !mbar_wait_warp(&full[kidx % S], (kidx / S) & 1, lim_ns, abort_flag)) {
                             ok = false;
                             break;
                         }

@@ -62,6 +62,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probes of three barriers issued back to back, so that their
+// shared-memory latencies overlap; r[i] is 1 when barrier i's phase with parity
+// q[i] is complete (acquire, like a completed wait).
+__device__ __forceinline__ void mbar_test3(uint64_t* b0, uint32_t q0, uint64_t* b1, uint32_t q1, uint64_t* b2,
+                                           uint32_t q2, uint32_t (&r)[3]) {
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, p2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p0, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p1, [%5], %6;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p2, [%7], %8;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\t"
+        "selp.u32 %1, 1, 0, p1;\n\t"
+        "selp.u32 %2, 1, 0, p2;\n\t}"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2])
+        : "r"(smem_u32(b0)), "r"(q0), "r"(smem_u32(b1)), "r"(q1), "r"(smem_u32(b2)), "r"(q2)
+        : "memory");
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // after `limit_ns` nanoseconds, or as soon as *abort is set by another role of
 // the same CTA; returns false in both cases.
