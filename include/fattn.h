@@ -81,6 +81,31 @@ fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int
                      fa_stream_t stream);
 
 /*
+ * fa_prefill_host -- fa_prefill with the inputs and the output in host memory.
+ * Passage: "FlashAttention-Style Kernels" (same computation as fa_prefill);
+ * the copies are the runtime around it.
+ *   q_host, k_host, v_host  bf16 [B, T, Hq|Hkv, d] in host memory (page-locked
+ *                           memory lets the copies overlap; pageable works)
+ *   out_host                bf16 [B, T, Hq, d] in host memory (written)
+ *   q, k, v, out            device buffers of the same shapes, with
+ *                           fa_prefill's alignment rules; the caller owns them
+ *                           and they are overwritten (q, k, v with the inputs)
+ * The batch is processed one sequence at a time: while sequence b is computed
+ * on `stream`, the inputs of b+1 are copied in and the output of b-1 is copied
+ * out on two library-owned streams, so copies in both directions overlap the
+ * kernels.  The output equals fa_prefill's for the whole batch bit for bit.
+ * Ordered on `stream` like any other call: it starts after the work already
+ * queued there, and work queued after it sees out_host written; the host is
+ * not synchronised.  No LSE output.  Errors: as fa_prefill, plus
+ * FA_ERR_INVALID_ARG for a NULL host pointer; FA_ERR_CUDA if a copy or event
+ * call fails while the pipeline is being queued (work queued before the
+ * failure still runs).
+ */
+fa_status fa_prefill_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                          void* q, void* k, void* v, void* out, int B, int T, int Hq, int Hkv, int d,
+                          int causal, float scale, fa_stream_t stream);
+
+/*
  * fa_prefill_masked -- as fa_prefill plus an additive mask M.
  * Passage: "FlashAttention-Style Kernels", attention equation with additive M.
  *   mask fp32 [T, T] row-major, broadcast over batch and heads; -inf allowed.

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libfattn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "cache_ops.cu", "paged.cu", "attn_tc.cu", "graph.cu", "block_pool.cpp"]
+SOURCES = ["api.cu", "cache_ops.cu", "paged.cu", "attn_tc.cu", "graph.cu", "host_pipeline.cu", "block_pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

@@ -30,7 +30,7 @@ EXPORTS = [
     "fa_cache_append_rope", "fa_decode_graph_create", "fa_decode_graph_launch", "fa_decode_graph_kernel_count",
     "fa_decode_graph_destroy", "fa_pool_create", "fa_pool_destroy", "fa_pool_add_seq", "fa_pool_fork",
     "fa_pool_append", "fa_pool_release", "fa_pool_tables", "fa_pool_num_free", "fa_pool_refcount", "fa_pool_seq_len",
-    "fa_copy_blocks", "fa_cache_append_fp8", "fa_paged_attn_fp8",
+    "fa_copy_blocks", "fa_cache_append_fp8", "fa_paged_attn_fp8", "fa_prefill_host",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
@@ -50,6 +50,7 @@ def _load() -> ctypes.CDLL:
     sig = {
         "fa_status_string": (ctypes.c_char_p, [I]),
         "fa_prefill": (I, [P, P, P, P, I, I, I, I, I, I, F, P, P]),
+        "fa_prefill_host": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]),
         "fa_prefill_masked_workspace_size": (Z, [I]),
         "fa_prefill_masked": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, Z, P]),
         "fa_stage_bf16": (I, [P, P, Z, P]),
@@ -147,6 +148,29 @@ def fa_prefill(q, k, v, causal: bool = True, scale: float | None = None, out=Non
     _check(_lib.fa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, d, int(causal), float(scale),
                            _ptr(lse), _stream(stream)), "fa_prefill")
     return out
+
+
+def fa_prefill_host(q_host, k_host, v_host, out_host, q, k, v, out, causal: bool = True,
+                    scale: float | None = None, stream=None):
+    """fa_prefill from and to host memory: the host tensors (bf16, contiguous,
+    ideally pinned) are copied into the caller's device buffers q/k/v and the
+    result back into out_host, one sequence at a time, with the copies
+    overlapping the kernels.  Ordered on `stream`; the host is not synchronised."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _need(t, n, torch.bfloat16, 4)
+    for n, t, dev in (("q_host", q_host, q), ("k_host", k_host, k), ("v_host", v_host, v), ("out_host", out_host, out)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise ValueError(f"{n} must be a host tensor")
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != dev.shape:
+            raise ValueError(f"{n} must be a contiguous bf16 tensor shaped like its device buffer")
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(_lib.fa_prefill_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), out_host.data_ptr(),
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, d, int(causal), float(scale),
+                                _stream(stream)), "fa_prefill_host")
+    return out_host
 
 
 def fa_prefill_masked_workspace_size(T: int) -> int:

@@ -56,6 +56,17 @@ def test_host_validation(fattn):
     # outputs must be 32-byte aligned; non-positive scale is rejected
     assert lib.fa_prefill(dummy, dummy, dummy, P(4096 + 16), 1, 16, 4, 2, 64, 1, 0.1, None, None) == fattn.FA_ERR_INVALID_ARG
     assert lib.fa_prefill(dummy, dummy, dummy, dummy, 1, 16, 4, 2, 64, 1, 0.0, None, None) == fattn.FA_ERR_INVALID_ARG
+    # host-buffer prefill: the same rules, plus every host pointer must be given
+    H = lambda *a: lib.fa_prefill_host(*a)
+    d8 = [dummy] * 8
+    assert H(*d8, -1, 16, 4, 2, 64, 1, 0.1, None) == fattn.FA_ERR_INVALID_ARG
+    assert H(*d8, 1, 16, 4, 2, 96, 1, 0.1, None) == fattn.FA_ERR_UNSUPPORTED
+    assert H(*([None] * 8), 0, 16, 4, 2, 64, 1, 0.1, None) == fattn.FA_OK
+    assert H(None, *d8[1:], 1, 16, 4, 2, 64, 1, 0.1, None) == fattn.FA_ERR_INVALID_ARG
+    assert H(*d8[:3], None, *d8[4:], 1, 16, 4, 2, 64, 1, 0.1, None) == fattn.FA_ERR_INVALID_ARG
+    assert H(*d8[:4], P(4097), *d8[5:], 1, 16, 4, 2, 64, 1, 0.1, None) == fattn.FA_ERR_INVALID_ARG
+    assert H(*d8[:7], P(4096 + 16), 1, 16, 4, 2, 64, 1, 0.1, None) == fattn.FA_ERR_INVALID_ARG
+    assert H(*d8, 1, 16, 4, 2, 64, 1, float("inf"), None) == fattn.FA_ERR_INVALID_ARG
     # paged: block size other than 16 is unsupported
     assert lib.fa_paged_attn(dummy, dummy, dummy, dummy, dummy, dummy, dummy, 2, 4, 8, 4, 2, 64, 32, 1, 0.1, 2, 1,
                              dummy, 1 << 20, None) == fattn.FA_ERR_UNSUPPORTED
