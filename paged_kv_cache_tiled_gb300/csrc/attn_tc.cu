@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* qfull = empty + S;
     uint64_t* qempty = qfull + 2;
     uint64_t* sfull = qempty + 2;
-    uint64_t* pfull = sfull + 2;  // [slot * 2 + half]: P columns of that half written (and O rescaled)
+    uint64_t* pfull = sfull + 2;  // [slot * 2 + half]: P columns of that half written (and O rescaled);
+                                  // the MMA warp waits on half 1, signalled after half 0
     uint64_t* ofull = pfull + 4;
     uint64_t* drain = ofull + 2;
     uint64_t* never = drain + 1;  // nothing arrives on it (forced time-out test hook)
@@ -711,9 +712,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const bool rescale_o = warp_rescale && it > 0;
                 // pass 2: P = 2^(logit - m) as bf16.  Half h reads S columns
                 // [64h, 64h+64) and writes P columns [32h, 32h+32), only over S
-                // columns already read; without a rescale each half goes to the MMA
-                // warp as soon as it is stored, so P*V over keys 0..63 overlaps half 1.
-                // column pairs go through packed f32x2 FMA / add (one instruction per pair)
+                // columns already read.  Without a rescale each half is signalled as
+                // soon as it is stored; the MMA warp waits on the second half only
+                // (one barrier check instead of two), but signalling the first
+                // half early, with its store wait, measured faster than one
+                // signal at the end.  Column pairs go through packed f32x2 FMA /
+                // add (one instruction per pair).
                 float2 rsp[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
                 const float sc = general ? 1.f : p.scale_log2;  // logits already scaled in the general case
