@@ -557,7 +557,8 @@ def main():
                     "gpu_launches": r5["launches"], "algorithmic_flops": f5, "algorithmic_bytes": b5,
                     "roofline": {"bound": "tensor" if f5 / (tc_peak * 1e12) > b5 / (hbm * 1e9) else "hbm",
                                  "achieved": tf5, "peak": tc_peak, "unit": "TFLOP/s",
-                                 "frac": t_bound / (r5["ms"] * 1e-3), "traffic": None,
+                                 "frac": t_bound / (r5["ms"] * 1e-3), "traffic": traffic.get("attn_tc_paged_c5"),
+                                 "kernel": "attn_tc_kernel<128, paged> (traffic: that launch alone)",
                                  "note": "frac = max(F/P_tc, B/BW) / measured time"}})
         # rotary embedding fused with the append, at config 5's chunk size
         rc = W.rope_case(21, 4096, 32, 8, 128, num_blocks=20000, max_pos=8704)
