@@ -504,3 +504,93 @@ def test_fp8_paged_oracle_equals_bf16_on_representable_values(k_scale, v_scale):
     got, lse = oracle.paged_attention_fp8(p.q, k8, v8, k_scale, v_scale, p.block_table, p.ctx_lens, p.q_lens, True,
                                           p.scale)
     assert np.array_equal(got, ref) and np.array_equal(lse, lse_ref)
+
+
+# ------------------------------------------------- sampled-row drivers ----
+# The full-size parity checks (the 16384-token prefill, the chunked prefill
+# over the paged cache, the sampled 8-bit decode) compare the GPU against the
+# oracle's row-by-row entry points, which have their own indexing: they pick a
+# (batch, head, row) or (sequence, row in chunk, head) triple, reuse the K/V of
+# the previous row when the (batch or sequence, kv head) repeats, and place
+# each row's output and LSE by its position in the request list.  These tests
+# pin them to the full-matrix functions pinned above: every requested row must
+# equal the corresponding row of the full result bit for bit (both evaluate the
+# attention equation of "FlashAttention-Style Kernels" with the same fp64
+# operations for that row).  The row lists revisit a (batch, kv head) out of
+# order, switch between query heads of one group, and interleave sequences, so
+# that a stale K/V reuse, a swapped head/row field or a misplaced LSE fails.
+
+def _revisiting_rows(rng, n, dims):
+    """n random index triples inside dims, plus runs that stay on one leading
+    index while the other two change, in a shuffled order."""
+    rows = [tuple(int(rng.integers(0, m)) for m in dims) for _ in range(n)]
+    a = int(rng.integers(0, dims[0]))
+    for x in range(dims[1]):
+        rows.append((a, x, int(rng.integers(0, dims[2]))))
+    rows += rows[:5]                      # repeated requests are answered again
+    order = rng.permutation(len(rows))
+    return np.array([rows[i] for i in order], dtype=np.int32)
+
+
+@pytest.mark.parametrize("causal,mask_kind,nthreads", [(True, "random", 1), (True, None, 3),
+                                                       (False, "band", 2), (False, None, 1)])
+def test_attention_rows_equal_full_matrix_rows(causal, mask_kind, nthreads):
+    B, Tq, Tk, Hq, Hkv, d = 2, 37, 53, 6, 2, 16          # Tq < Tk (bottom-right), g = 3
+    q = W.normal_tensor(41, W.S_Q, (B, Tq, Hq, d))
+    k = W.normal_tensor(41, W.S_K, (B, Tk, Hkv, d))
+    v = W.normal_tensor(41, W.S_V, (B, Tk, Hkv, d))
+    mask = None if mask_kind is None else W.make_mask(mask_kind, Tq, Tk, 41)
+    full, lse_full = oracle.attention(q, k, v, causal, 0.3, mask=mask)
+    rows = _revisiting_rows(np.random.default_rng(5), 60, (B, Hq, Tq))   # (b, h, i)
+    got, lse = oracle.attention_rows(q, k, v, causal, 0.3, rows, mask=mask, nthreads=nthreads)
+    b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
+    assert np.array_equal(got, full[b, i, h])
+    assert np.array_equal(lse, lse_full[b, h, i])
+    with pytest.raises(RuntimeError):      # a row outside the problem is an error, not a read
+        oracle.attention_rows(q, k, v, causal, 0.3, np.array([[0, Hq, 0]], np.int32), mask=mask)
+
+
+@pytest.mark.parametrize("nthreads", [1, 4])
+def test_paged_attention_rows_equal_full_rows(nthreads):
+    # mixed chunks: decode (1), a chunk longer than 16, a chunk spanning blocks, an empty context
+    ctx_old, qlen = [37, 0, 80, 5, 130], [1, 17, 23, 1, 40]
+    p = W.paged_case(43, ctx_old, qlen, 6, 2, 16, num_blocks=60, perm_seed=44)
+    kc, vc = oracle.cache_append(p.k_new, p.v_new, p.slot_mapping, oracle.to_bits(p.k_cache),
+                                 oracle.to_bits(p.v_cache))
+    full, lse_full = oracle.paged_attention(p.q, kc, vc, p.block_table, p.ctx_lens, p.q_lens,
+                                            True, p.scale)
+    rng = np.random.default_rng(6)
+    rows = [(s, int(rng.integers(0, qlen[s])), int(rng.integers(0, 6)))
+            for s in rng.integers(0, len(qlen), 70)]
+    rows += [(4, qi, h) for h in (5, 0, 3) for qi in (39, 0, 17)]          # one sequence, heads out of order
+    rows = np.array([rows[i] for i in rng.permutation(len(rows))], dtype=np.int32)
+    got, lse = oracle.paged_attention_rows(p.q, kc, vc, p.block_table, p.ctx_lens, p.q_lens, True,
+                                           p.scale, rows, nthreads=nthreads)
+    q_start = np.concatenate([[0], np.cumsum(qlen)])
+    t = q_start[rows[:, 0]] + rows[:, 1]
+    assert np.array_equal(got, full[t, rows[:, 2]])
+    assert np.array_equal(lse, lse_full[t, rows[:, 2]])
+    with pytest.raises(RuntimeError):      # a row past its sequence's chunk is an error
+        oracle.paged_attention_rows(p.q, kc, vc, p.block_table, p.ctx_lens, p.q_lens, True, p.scale,
+                                    np.array([[0, 1, 0]], np.int32))
+
+
+def test_fp8_paged_attention_rows_equal_full_rows():
+    ctx_old, qlen = [40, 3, 130, 0], [1, 2, 17, 9]
+    p = W.paged_case(45, ctx_old, qlen, 8, 2, 32, num_blocks=40)
+    rng = np.random.default_rng(7)
+    k_all = torch.from_numpy(rng.standard_normal((40 * 16, 2, 32)).astype(np.float32))
+    v_all = torch.from_numpy(rng.standard_normal((40 * 16, 2, 32)).astype(np.float32))
+    k8, v8 = oracle.cache_append_fp8(k_all, v_all, torch.arange(40 * 16, dtype=torch.int32),
+                                     np.zeros((40, 2, 16, 32), np.uint8), np.zeros((40, 2, 32, 16), np.uint8),
+                                     0.5, 2.0)
+    full, lse_full = oracle.paged_attention_fp8(p.q, k8, v8, 0.5, 2.0, p.block_table, p.ctx_lens, p.q_lens,
+                                                True, p.scale)
+    rows = np.array([(s, int(rng.integers(0, qlen[s])), int(rng.integers(0, 8)))
+                     for s in rng.integers(0, 4, 50)] + [(2, 16, 7), (2, 0, 0), (2, 16, 1)], dtype=np.int32)
+    got, lse = oracle.paged_attention_fp8(p.q, k8, v8, 0.5, 2.0, p.block_table, p.ctx_lens, p.q_lens, True,
+                                          p.scale, rows=rows, nthreads=3)
+    q_start = np.concatenate([[0], np.cumsum(qlen)])
+    t = q_start[rows[:, 0]] + rows[:, 1]
+    assert np.array_equal(got, full[t, rows[:, 2]])
+    assert np.array_equal(lse, lse_full[t, rows[:, 2]])
