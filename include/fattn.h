@@ -122,6 +122,21 @@ fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const f
                             fa_stream_t stream);
 
 /*
+ * fa_mask_tile_classes -- classes of the 128 x 128 tiles of an additive mask
+ * (the first pass of fa_prefill_masked, callable alone).
+ * Passage: "FlashAttention-Style Kernels", attention equation with additive M
+ * (a tile of M that is -inf everywhere contributes nothing; a tile that is 0
+ * everywhere leaves the scores unchanged).
+ *   mask fp32 [Tq, Tk] row-major, 16-byte aligned
+ *   cls  uint8 [ceil(Tq/128), ceil(Tk/128)] row-major (written): 0 when every
+ *        in-range element of the tile is -inf, 1 when every one is exactly 0
+ *        (either sign), 2 otherwise; edge tiles cover only in-range elements
+ * One read of M.  Empty masks are a no-op.  FA_ERR_UNSUPPORTED when Tq needs
+ * more than 65535 tile rows.
+ */
+fa_status fa_mask_tile_classes(const float* mask, int Tq, int Tk, uint8_t* cls, fa_stream_t stream);
+
+/*
  * fa_stage_bf16 -- fp32 -> bf16 conversion, round to nearest even.  Used to
  * stage fp32 q/k/v for the bf16 attention kernels.
  *   src fp32 [n], dst bf16 [n]; both 16-byte aligned.

@@ -1,6 +1,8 @@
 // libfattn host runtime: status strings, the per-device error word, device
 // checks, tensor-map encoding and the debug wait bound.
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "host_common.cuh"
 
@@ -14,6 +16,9 @@ std::mutex g_mu;
 unsigned* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, 2 unsupported
+// kernels whose dynamic shared-memory limit has been raised, per device:
+// (kernel, bytes) pairs (the attribute is a per-device setting)
+std::vector<std::pair<const void*, int>> g_smem_attr[kMaxDevices];
 unsigned long long g_wait_ns = 4000000000ull;
 int g_force_timeout = 0;
 thread_local int t_launches = 0;
@@ -84,6 +89,18 @@ fa_status check_device() {
         g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
     }
     return g_arch_ok[dev] == 1 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+fa_status raise_dynamic_smem(const void* kernel, int bytes) {
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const auto& e : g_smem_attr[dev])
+        if (e.first == kernel && e.second >= bytes) return FA_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return FA_ERR_CUDA;
+    g_smem_attr[dev].emplace_back(kernel, bytes);
+    return FA_OK;
 }
 
 void set_launch_count(int n) { t_launches = n; }

@@ -856,13 +856,8 @@ fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, cud
 template <int D, int MODE>
 static fa_status launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcParams& p,
                            int grid, cudaStream_t s, const TcSched& sched) {
-    static bool attr_done = false;  // setting the attribute twice is harmless
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(attn_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcCfg<D>::kSmem) != cudaSuccess)
-            return FA_ERR_CUDA;
-        attr_done = true;
-    }
+    const fa_status st = raise_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel<D, MODE>), TcCfg<D>::kSmem);
+    if (st != FA_OK) return st;
     attn_tc_kernel<D, MODE><<<grid, kTcThreads, TcCfg<D>::kSmem, s>>>(tq, tk, tv, p, sched);
     return cuda_status(cudaGetLastError());
 }
@@ -1092,9 +1087,8 @@ fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const f
     if ((st = launch_mask_classify(mask, T, T, cls, s)) != FA_OK) return st;
     if ((size_t)nt * sizeof(int) > 200 * 1024) return FA_ERR_UNSUPPORTED;
     if (nt * sizeof(int) > 48 * 1024 &&
-        cudaFuncSetAttribute(mask_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, nt * (int)sizeof(int)) !=
-            cudaSuccess)
-        return FA_ERR_CUDA;
+        (st = raise_dynamic_smem(reinterpret_cast<const void*>(mask_order_kernel), nt * (int)sizeof(int))) != FA_OK)
+        return st;
     mask_order_kernel<<<1, 256, nt * sizeof(int), s>>>(cls, nt, nt, causal ? 1 : 0, order, range);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     TcParams p = base_params(B, T, Hq, Hkv, causal, scale, out, lse, ctx);

@@ -347,6 +347,19 @@ fa_status fa_cache_append(const void* k, const void* v, void* k_cache, void* v_c
     return st;
 }
 
+fa_status fa_mask_tile_classes(const float* mask, int Tq, int Tk, uint8_t* cls, fa_stream_t stream) {
+    set_launch_count(0);
+    if (Tq < 0 || Tk < 0) return FA_ERR_INVALID_ARG;
+    if (Tq == 0 || Tk == 0) return FA_OK;
+    if (!mask || !cls || !aligned16(mask)) return FA_ERR_INVALID_ARG;
+    if ((Tq + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;  // grid y limit
+    fa_status st = check_device();
+    if (st != FA_OK) return st;
+    st = launch_mask_classify(mask, Tq, Tk, cls, reinterpret_cast<cudaStream_t>(stream));
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
 fa_status fa_stage_bf16(const float* src, void* dst, size_t n, fa_stream_t stream) {
     set_launch_count(0);
     if (n == 0) return FA_OK;

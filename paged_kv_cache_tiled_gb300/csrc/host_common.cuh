@@ -22,6 +22,10 @@ int sm_count();
 // Returns FA_OK when the current device is an sm_103 part.
 fa_status check_device();
 
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the
+// current device, once per (device, kernel); thread-safe.
+fa_status raise_dynamic_smem(const void* kernel, int bytes);
+
 // Records how many kernels the current API call launched (per host thread).
 void set_launch_count(int n);
 

@@ -599,8 +599,7 @@ constexpr int kMergeMaxThreads = 32 * kDecodeRows;
 template <int D>
 __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
                                                                     const int32_t* __restrict__ q_lens,
-                                                                    const float* __restrict__ part_o,
-                                                                    const float2* __restrict__ part_ml,
+                                                                    const float* part_o, const float2* part_ml,
                                                                     uint16_t* __restrict__ out, int num_seqs,
                                                                     int Hq, int Hkv, int mbps, int W) {
     // one warp per output row: warp w of CTA (s, hk) merges row w
@@ -657,7 +656,9 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
     // max of earlier groups rescales the accumulators
     for (int c0 = 0; c0 < npieces; c0 += 32) {
         const long myslot = c0 + lane < npieces ? (c0 == 0 ? lane_slot : slot_of(c0 + lane)) : -1;
-        const float2 ml = myslot >= 0 ? part_ml[myslot * kDecodeRows + r] : make_float2(-INFINITY, 0.f);
+        // partials are read through L2 (ld.global.cg): the decode grid wrote them
+        // while this grid was already resident, so the read-only path is not valid
+        const float2 ml = myslot >= 0 ? __ldcg(part_ml + myslot * kDecodeRows + r) : make_float2(-INFINITY, 0.f);
         float gm = ml.x;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
@@ -681,10 +682,10 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
                 const long sj = __shfl_sync(0xffffffffu, myslot, j + u);
                 const float* src = part_o + ((sj < 0 ? 0 : sj) * kDecodeRows + r) * D + lane * kPer;
                 if constexpr (kPer == 4) {
-                    const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+                    const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
                     v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
                 } else {
-                    const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+                    const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
                     v[u][0] = t.x; v[u][1] = t.y;
                 }
                 if (sj < 0)  // an empty range wrote no partial: ignore whatever the slot holds
@@ -702,7 +703,7 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
             if (sj < 0) continue;  // uniform across the warp
             const float* src = part_o + (sj * kDecodeRows + r) * D + lane * kPer;
 #pragma unroll
-            for (int c = 0; c < kPer; ++c) acc[c] += wj * __ldg(src + c);
+            for (int c = 0; c < kPer; ++c) acc[c] += wj * __ldcg(src + c);
         }
     }
 #pragma unroll
@@ -836,13 +837,8 @@ static fa_status launch_decode(const void* q, const void* k_cache, const void* v
         if ((st = encode_tmap_bf16_4d(&tv, v_cache, dims, strides, box)) != FA_OK) return st;
     }
     using L = StreamSmem<D, KV8>;
-    static bool attr_done = false;  // benign race: setting the attribute twice is harmless
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(paged_decode_kernel<D, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) !=
-            cudaSuccess)
-            return FA_ERR_CUDA;
-        attr_done = true;
-    }
+    if ((st = raise_dynamic_smem(reinterpret_cast<const void*>(paged_decode_kernel<D, KV8>), L::kBytes)) != FA_OK)
+        return st;
     float* part_o = reinterpret_cast<float*>(ws + w.part_o);
     float2* part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
     const float scale_log2 = scale * k_scale * 1.4426950408889634f;
@@ -922,9 +918,8 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
         const size_t hist_bytes = sizeof(int) * (size_t)(nbins + 1);
         if (hist_bytes > 200 * 1024) return FA_ERR_UNSUPPORTED;
         if (hist_bytes > 48 * 1024 &&
-            cudaFuncSetAttribute(paged_meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes) !=
-                cudaSuccess)
-            return FA_ERR_CUDA;
+            (st = raise_dynamic_smem(reinterpret_cast<const void*>(paged_meta_kernel), (int)hist_bytes)) != FA_OK)
+            return st;
         paged_meta_kernel<<<1, 1024, hist_bytes, s>>>(ctx_lens, q_lens, num_seqs, max_blocks_per_seq, g, causal,
                                                       tiles_per_entry, q_start, count, list, w.max_entries, ctx);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;

@@ -30,7 +30,7 @@ EXPORTS = [
     "fa_cache_append_rope", "fa_decode_graph_create", "fa_decode_graph_launch", "fa_decode_graph_kernel_count",
     "fa_decode_graph_destroy", "fa_pool_create", "fa_pool_destroy", "fa_pool_add_seq", "fa_pool_fork",
     "fa_pool_append", "fa_pool_release", "fa_pool_tables", "fa_pool_num_free", "fa_pool_refcount", "fa_pool_seq_len",
-    "fa_copy_blocks", "fa_cache_append_fp8", "fa_paged_attn_fp8", "fa_prefill_host",
+    "fa_copy_blocks", "fa_cache_append_fp8", "fa_paged_attn_fp8", "fa_prefill_host", "fa_mask_tile_classes",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "fa_prefill_masked_workspace_size": (Z, [I]),
         "fa_prefill_masked": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, Z, P]),
         "fa_stage_bf16": (I, [P, P, Z, P]),
+        "fa_mask_tile_classes": (I, [P, I, I, P, P]),
         "fa_cache_append": (I, [P, P, P, P, P, I, I, I, I, I, P]),
         "fa_paged_attn_workspace_size": (Z, [I, I, I, I, I, I]),
         "fa_paged_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, Z, P]),
@@ -195,6 +196,20 @@ def fa_prefill_masked(q, k, v, mask, causal: bool = False, scale: float | None =
     _check(_lib.fa_prefill_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), B, T, Hq, Hkv, d, int(causal),
                                   float(scale), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
                                   _stream(stream)), "fa_prefill_masked")
+    return out
+
+
+def fa_mask_tile_classes(mask, out=None, stream=None):
+    """uint8 [ceil(Tq/128), ceil(Tk/128)] classes of an fp32 mask [Tq, Tk]: 0 all -inf, 1 all zero, 2 mixed."""
+    _need(mask, "mask", torch.float32, 2)
+    Tq, Tk = mask.shape
+    shape = ((Tq + 127) // 128, (Tk + 127) // 128)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.uint8, device=mask.device)
+    _need(out, "out", torch.uint8, 2)
+    if tuple(out.shape) != shape:
+        raise ValueError(f"out must have shape {shape}")
+    _check(_lib.fa_mask_tile_classes(_ptr(mask), Tq, Tk, _ptr(out), _stream(stream)), "fa_mask_tile_classes")
     return out
 
 

@@ -108,3 +108,18 @@ def test_mask_tile_classes_match_oracle(F, T, kind):
     nt = (T + 127) // 128
     got = ws[: nt * nt].cpu().numpy().reshape(nt, nt)
     assert np.array_equal(got, oracle.mask_tile_classes(case.mask))
+
+
+@pytest.mark.parametrize("Tq,Tk", [(300, 300), (128, 640), (257, 129), (1, 3)])
+@pytest.mark.parametrize("kind", ["random", "band", "causal_inf"])
+def test_mask_tile_classes_entry_point(F, Tq, Tk, kind):
+    """The standalone class pass equals the oracle on ragged and non-square masks."""
+    mask = W.make_mask(kind, Tq, Tk, 11)
+    if kind == "random":  # plant all-zero and all--inf tiles among the mixed ones
+        mask[:128, :128] = 0.0
+        if Tk > 128:
+            mask[:, 128:256] = float("-inf")
+    got = F.fa_mask_tile_classes(mask.cuda())
+    assert F.fa_get_error() == F.FA_OK
+    assert np.array_equal(got.cpu().numpy(), oracle.mask_tile_classes(mask))
+
