@@ -79,22 +79,6 @@ inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, i
     return w;
 }
 
-// Sum of q_lens[0..s) by the whole CTA (blockDim.x threads, multiple of 32).
-__device__ int cta_prefix(const int32_t* __restrict__ q_lens, int s, int* red) {
-    int acc = 0;
-    for (int i = threadIdx.x; i < s; i += blockDim.x) acc += __ldg(q_lens + i);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[w] = acc;
-    __syncthreads();
-    int tot = 0;
-    for (int i = 0; i < nw; ++i) tot += red[i];
-    __syncthreads();
-    return tot;
-}
-
 // -------------------------------------------------------------- decode -----
 // Work is balanced by pages: the decode segments (sequence, kv head) are laid
 // end to end, sequence-major, as one stream of 16-token pages; warp w of the
@@ -133,20 +117,6 @@ struct StreamSplit {
     }
 };
 
-// Sum over the CTA (blockDim.x a multiple of 32, at most 32 warps).
-__device__ long long cta_sum_ll(long long v, long long* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[w] = v;
-    __syncthreads();
-    long long t = 0;
-    for (int i = 0; i < nw; ++i) t += red[i];
-    __syncthreads();
-    return t;
-}
-
 // KV8: the 8-bit (E4M3) cache; its pages are half the bytes, so the ring is
 // twice as deep to keep the same bytes in flight.
 template <int D, bool KV8 = false>
@@ -156,7 +126,7 @@ struct StreamSmem {
     static constexpr int kStages = KV8 ? 2 * kStreamStages : kStreamStages;
     static constexpr int kRing = kStreamWarps * kStages * kStage;
     static constexpr int kBars = kStreamWarps * kStages + 1;
-    static constexpr int kBytes = 1024 /*align slack*/ + kRing + kBars * 8 + 512;
+    static constexpr int kBytes = 1024 /*align slack*/ + kRing + kBars * 8 + 64;
 };
 
 // Position of a stream cursor: sequence, kv head, block within the sequence.
@@ -175,14 +145,15 @@ struct Cursor {
 // = elements (4t .. 4t+3); queries are loaded in the same order for Q K^T,
 // and for P V the S tile's columns (tokens) are produced in that order by
 // loading K rows 4t+2nt+e into n-tile nt, column 2t+e.
+constexpr int kLensPerLane = 8;  // sequences per lane whose lengths are loaded in one batch
 template <int D, bool KV8 = false>
 __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const uint16_t* __restrict__ q, const int32_t* __restrict__ bt,
                         const int32_t* __restrict__ ctx_lens, const int32_t* __restrict__ q_lens,
                         uint16_t* __restrict__ out, float* __restrict__ part_o, float2* __restrict__ part_ml,
-                        int num_seqs, int mbps, int num_blocks, int Hq, int Hkv, int causal, float scale_log2,
-                        float v_scale, DevCtx ctx) {
+                        int num_seqs, int mbps, int num_blocks, int Hq, int Hkv, int q_prefetch_rows, int causal,
+                        float scale_log2, float v_scale, DevCtx ctx) {
     // the merge kernel that follows may be scheduled now; it waits for this
     // grid's completion before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -192,101 +163,113 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kRing);
     uint64_t* never = bars + kStreamWarps * kStreamStages;  // nothing arrives on it (time-out test hook)
-    long long* red = reinterpret_cast<long long*>(never + 1);  // 2 * kStreamWarps entries
-    int* start_s = reinterpret_cast<int*>(red + 2 * kStreamWarps);  // per warp: first sequence, page offset, q0
-    int* start_off = start_s + kStreamWarps;
-    int* start_q0 = start_off + kStreamWarps;
-    volatile int* abort_flag = start_q0 + kStreamWarps;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(never + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = Hq / Hkv;
     const int W = gridDim.x * kStreamWarps;
     const int gw = blockIdx.x * kStreamWarps + warp;
     if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
         for (int i = 0; i < L::kBars; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (threadIdx.x < kStreamWarps) start_s[threadIdx.x] = -1;
-
-    // pass 1: total pages P (and length checks).  With at most blockDim.x
-    // sequences each thread keeps its sequence's values for pass 2.
-    long long mine = 0;
-    const bool one_chunk = num_seqs <= (int)blockDim.x;
-    long long my_n = 0, my_q = 0;
-    if (one_chunk && threadIdx.x < num_seqs) {
-        my_n = (long long)Hkv * decode_blocks(q_lens, ctx_lens, threadIdx.x, g, mbps);
-        my_q = __ldg(q_lens + threadIdx.x);
+    {
+        // warm L2 with this CTA's share of the block table and (when every
+        // query row is a decode row) of the queries, read right after the lengths
+        constexpr long kMaxPrefetchLines = (4L << 20) / 128;  // 4 MB each at most
+        const long tb_lines = min(kMaxPrefetchLines, ((long)num_seqs * mbps * 4 + 127) / 128);
+        const long q_lines = min(kMaxPrefetchLines, ((long)q_prefetch_rows * Hq * D * 2 + 127) / 128);
+        const long tb_lo = tb_lines * blockIdx.x / gridDim.x, tb_hi = tb_lines * (blockIdx.x + 1) / gridDim.x;
+        const long q_lo = q_lines * blockIdx.x / gridDim.x, q_hi = q_lines * (blockIdx.x + 1) / gridDim.x;
+        for (long i = tb_lo + threadIdx.x; i < tb_hi; i += blockDim.x)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(bt) + i * 128));
+        for (long i = q_lo + threadIdx.x; i < q_hi; i += blockDim.x)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(q) + i * 128));
     }
-    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
-        const int ql = __ldg(q_lens + s), cl = __ldg(ctx_lens + s);
-        if (!is_decode_row(ql, g)) continue;
+
+    // Where this warp's pages start.  Every warp finds out on its own (no
+    // CTA-wide step on the path to the first copy): lane j sums the decode
+    // pages and the query rows of sequences [j*per, (j+1)*per), and a warp
+    // scan gives each lane's offsets and the total P.
+    const int per = (num_seqs + 31) >> 5;
+    const int s_lo = min(num_seqs, lane * per), s_hi = min(num_seqs, s_lo + per);
+    long long my_p = 0, my_q = 0;
+    bool bad = false;
+    auto count = [&](int ql, int cl) {
+        my_q += ql;
+        if (!is_decode_row(ql, g)) return;
         if (ql > cl || cl > mbps * kBS) {
-            if (blockIdx.x == 0) raise_error(ctx, ERR_BOUNDS_BIT);
-            continue;
+            bad = true;
+            return;
         }
-        mine += (cl + kBS - 1) / kBS;
+        my_p += (long long)Hkv * ((cl + kBS - 1) / kBS);
+    };
+    if (per <= kLensPerLane) {
+        int qv[kLensPerLane], cv[kLensPerLane];
+#pragma unroll
+        for (int i = 0; i < kLensPerLane; ++i) {  // all loads issued before any is used
+            const bool in = s_lo + i < s_hi;
+            qv[i] = in ? __ldg(q_lens + s_lo + i) : 0;
+            cv[i] = in ? __ldg(ctx_lens + s_lo + i) : 0;
+        }
+        __syncthreads();  // barrier initialisation visible to every warp (the loads are in flight)
+#pragma unroll
+        for (int i = 0; i < kLensPerLane; ++i)
+            if (s_lo + i < s_hi) count(qv[i], cv[i]);
+    } else {
+        __syncthreads();
+#pragma unroll 4
+        for (int s = s_lo; s < s_hi; ++s) count(__ldg(q_lens + s), __ldg(ctx_lens + s));
     }
-    const long long P = (long long)Hkv * cta_sum_ll(mine, red);
-    // pass 2: locate the first page of this CTA's warps (prefix scan over sequences)
+    if (bad && gw == 0) raise_error(ctx, ERR_BOUNDS_BIT);
+    long long inc_p = my_p, inc_q = my_q;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long yp = __shfl_up_sync(0xffffffffu, inc_p, o), yq = __shfl_up_sync(0xffffffffu, inc_q, o);
+        if (lane >= o) {
+            inc_p += yp;
+            inc_q += yq;
+        }
+    }
+    const long long P = __shfl_sync(0xffffffffu, inc_p, 31);
+    if (P == 0) return;
     const StreamSplit split(P, W);
-    long long first[kStreamWarps];
-#pragma unroll
-    for (int i = 0; i < kStreamWarps; ++i) first[i] = split.begin(blockIdx.x * kStreamWarps + i);
-    const long long cta_end = split.begin((blockIdx.x + 1) * kStreamWarps);
-    long long carry_p = 0, carry_q = 0;
-    for (int base = 0; base < num_seqs && carry_p < cta_end; base += blockDim.x) {
-        const int s = base + threadIdx.x;
-        long long n = 0, ql = 0;
-        if (one_chunk) {
-            n = my_n;
-            ql = my_q;
-        } else if (s < num_seqs) {
-            n = (long long)Hkv * decode_blocks(q_lens, ctx_lens, s, g, mbps);
-            ql = __ldg(q_lens + s);
-        }
-        // inclusive scans of pages and query rows within this chunk
-        long long xp = n, xq = ql;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long yp = __shfl_up_sync(0xffffffffu, xp, o), yq = __shfl_up_sync(0xffffffffu, xq, o);
-            if (lane >= o) {
-                xp += yp;
-                xq += yq;
-            }
-        }
-        __syncthreads();
-        if (lane == 31) {
-            red[warp] = xp;
-            red[kStreamWarps + warp] = xq;
-        }
-        __syncthreads();
-        long long off_p = carry_p, off_q = carry_q, tot_p = 0, tot_q = 0;
-        for (int i = 0; i < kStreamWarps; ++i) {
-            if (i < warp) {
-                off_p += red[i];
-                off_q += red[kStreamWarps + i];
-            }
-            tot_p += red[i];
-            tot_q += red[kStreamWarps + i];
-        }
-        const long long excl_p = off_p + xp - n, excl_q = off_q + xq - ql;
-        if (n > 0)
-#pragma unroll
-            for (int i = 0; i < kStreamWarps; ++i)
-                if (first[i] >= excl_p && first[i] < excl_p + n) {
-                    start_s[i] = s;
-                    start_off[i] = (int)(first[i] - excl_p);
-                    start_q0[i] = (int)excl_q;
-                }
-        carry_p += tot_p;
-        carry_q += tot_q;
-    }
-    __syncthreads();
-
     const long long b0 = split.begin(gw), b1 = split.begin(gw + 1);
     const int n_pages = (int)(b1 - b0);
-    if (n_pages <= 0 || start_s[warp] < 0) return;  // no more CTA-wide synchronisation below
+    if (n_pages <= 0) return;  // no CTA-wide synchronisation below
+    // the lane whose sequences hold page b0 walks them (lengths are L1 hits now)
+    Cursor start;
+    {
+        const unsigned hit = __ballot_sync(0xffffffffu, my_p > 0 && b0 >= inc_p - my_p && b0 < inc_p);
+        const int src = __ffs(hit) - 1;  // exactly one lane: 0 <= b0 < P
+        int a_s = 0, a_off = 0, a_q0 = 0;
+        if (lane == src) {
+            long long off = b0 - (inc_p - my_p), q0 = inc_q - my_q;
+            for (int s = s_lo; s < s_hi; ++s) {
+                const int ql = __ldg(q_lens + s), cl = __ldg(ctx_lens + s);
+                const long long n =
+                    (is_decode_row(ql, g) && ql <= cl && cl <= mbps * kBS) ? (long long)Hkv * ((cl + kBS - 1) / kBS)
+                                                                            : 0;
+                if (off < n) {
+                    a_s = s;
+                    a_off = (int)off;
+                    a_q0 = (int)q0;
+                    break;
+                }
+                off -= n;
+                q0 += ql;
+            }
+        }
+        start.s = __shfl_sync(0xffffffffu, a_s, src);
+        a_off = __shfl_sync(0xffffffffu, a_off, src);
+        start.q0 = __shfl_sync(0xffffffffu, a_q0, src);
+        start.nblk = decode_blocks(q_lens, ctx_lens, start.s, g, mbps);
+        start.hk = a_off / start.nblk;
+        start.blk = a_off % start.nblk;
+    }
 
     uint8_t* ring = smem + warp * kStreamStages * L::kStage;
     uint64_t* wbar = bars + warp * kStreamStages;
@@ -303,12 +286,6 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
             c.nblk = c.s < num_seqs ? decode_blocks(q_lens, ctx_lens, c.s, g, mbps) : 0;
         } while (c.s < num_seqs && c.nblk == 0);
     };
-    Cursor start;
-    start.s = start_s[warp];
-    start.nblk = decode_blocks(q_lens, ctx_lens, start.s, g, mbps);
-    start.hk = start_off[warp] / start.nblk;
-    start.blk = start_off[warp] % start.nblk;
-    start.q0 = start_q0[warp];
 
     Cursor ci = start;  // issue cursor (lane 0 only)
     // lane 0 reads the block-table entry of the next page one issue ahead, so
@@ -810,8 +787,9 @@ __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restr
 template <int D, bool KV8 = false>
 static fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* bt,
                                const int32_t* ctx_lens, const int32_t* q_lens, void* out, const PagedWs& w,
-                               uint8_t* ws, int num_seqs, int mbps, int num_blocks, int Hq, int Hkv, int causal,
-                               float scale, int merge_rows, cudaStream_t s, const DevCtx& ctx, int* launches,
+                               uint8_t* ws, int num_seqs, int mbps, int num_blocks, int Hq, int Hkv,
+                               int q_prefetch_rows, int causal, float scale, int merge_rows, cudaStream_t s,
+                               const DevCtx& ctx, int* launches,
                                float k_scale = 1.f, float v_scale = 1.f) {
     CUtensorMap tk, tv;
     fa_status st;
@@ -845,7 +823,7 @@ static fa_status launch_decode(const void* q, const void* k_cache, const void* v
     const int grid = std::min(sm_count(), kMaxStreamCtas);
     paged_decode_kernel<D, KV8><<<grid, kStreamWarps * 32, L::kBytes, s>>>(
         tk, tv, static_cast<const uint16_t*>(q), bt, ctx_lens, q_lens, static_cast<uint16_t*>(out), part_o, part_ml,
-        num_seqs, mbps, num_blocks, Hq, Hkv, causal, scale_log2, v_scale, ctx);
+        num_seqs, mbps, num_blocks, Hq, Hkv, q_prefetch_rows, causal, scale_log2, v_scale, ctx);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     ++*launches;
     cudaLaunchConfig_t cfg = {};
@@ -901,12 +879,13 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
     int launches = 0;
     if (g <= kDecodeRows) {
         const int merge_rows = (int)std::min<long>(kDecodeRows, (long)g * max_q_len);
+        const int qpf = is_decode_row(max_q_len, g) ? total_q : 0;  // every query row is a decode row
         st = d == 128 ? launch_decode<128>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
-                                           max_blocks_per_seq, num_blocks, Hq, Hkv, causal, scale, merge_rows, s, ctx,
-                                           &launches)
+                                           max_blocks_per_seq, num_blocks, Hq, Hkv, qpf, causal, scale, merge_rows, s,
+                                           ctx, &launches)
                       : launch_decode<64>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
-                                          max_blocks_per_seq, num_blocks, Hq, Hkv, causal, scale, merge_rows, s, ctx,
-                                          &launches);
+                                          max_blocks_per_seq, num_blocks, Hq, Hkv, qpf, causal, scale, merge_rows, s,
+                                          ctx, &launches);
         if (st != FA_OK) return st;
     }
     if (!is_decode_row(max_q_len, g)) {
@@ -958,9 +937,9 @@ fa_status fa_paged_attn_fp8(const void* q, const void* k_cache, const void* v_ca
     if ((st = make_ctx(&ctx)) != FA_OK) return st;
     int launches = 0;
     st = launch_decode<128, true>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w,
-                                  static_cast<uint8_t*>(ws), num_seqs, max_blocks_per_seq, num_blocks, Hq, Hkv, causal,
-                                  scale, (Hq / Hkv) * max_q_len, reinterpret_cast<cudaStream_t>(stream), ctx,
-                                  &launches, k_scale, v_scale);
+                                  static_cast<uint8_t*>(ws), num_seqs, max_blocks_per_seq, num_blocks, Hq, Hkv,
+                                  total_q, causal, scale, (Hq / Hkv) * max_q_len,
+                                  reinterpret_cast<cudaStream_t>(stream), ctx, &launches, k_scale, v_scale);
     if (st != FA_OK) return st;
     set_launch_count(launches);
     return FA_OK;

@@ -197,3 +197,22 @@ def test_decode_workspace_needs_no_clearing(F):
         assert torch.equal(o, outs[0])
     ref, _, _ = oracle_paged(p, bits(kc), bits(vc))
     assert_parity(outs[0], ref, "decode, uncleared workspace")
+
+
+@pytest.mark.parametrize("route", ["decode", "mixed"])
+def test_empty_sequences_in_the_batch(F, route):
+    """Sequences with q_len = 0 -- with cached context, and with ctx_len = 0 --
+    sit between decode and chunk sequences: they produce no rows and read
+    nothing, every other row matches the oracle, and nothing outside the output
+    is written (guard bands).  A sequence with ctx_len = q_len = 1 (the first
+    token of a prompt) decodes against itself alone."""
+    if route == "decode":
+        ctx_old, ql = [0, 300, 0, 45, 1000, 0, 7, 2999], [0, 1, 0, 0, 1, 1, 0, 1]
+    else:
+        ctx_old, ql = [0, 300, 0, 45, 1000, 0, 7, 200, 0], [0, 1, 0, 0, 130, 1, 0, 3, 0]
+    p = W.paged_case(48, ctx_old, ql, 12, 2, 128, num_blocks=500)
+    out, kc, vc, st = run_paged(F, p, max_q_len=max(ql), out_guard=True)
+    assert st == F.FA_OK
+    ref, _, _ = oracle_paged(p, bits(kc), bits(vc))
+    assert_parity(out, ref, f"empty sequences ({route})")
+
