@@ -73,6 +73,8 @@ struct TcParams {
     int causal;
     float scale_log2;
     int pair_heads;  // 1: slots = heads (2pp, 2pp+1) of a group; 0: row tiles (2t, 2t+1) of one head
+    int pack;        // paged: a slot is 128/g tokens x the g heads of a group (row = token * g + head)
+    int pack_shift;  // log2(g) when packed
     int num_units;   // dense / masked
     uint16_t* out;
     float* lse;
@@ -141,31 +143,43 @@ __device__ __forceinline__ int cta_unit(const TcSched& sc, int i, int G, int num
     return u < num_units ? u : -1;
 }
 
+// Units of one paged work entry: one per kv head (packed), per head pair, or per head.
+__device__ __forceinline__ int paged_units_per_entry(const TcParams& p) {
+    return p.pack ? p.Hkv : (p.pair_heads ? p.Hkv * (p.g / 2) : p.Hq);
+}
+
 template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
     Unit U;
     if constexpr (MODE == MODE_PAGED) {
-        const int per_entry = p.pair_heads ? p.Hkv * (p.g / 2) : p.Hq;
+        const int per_entry = paged_units_per_entry(p);
         const int e = u / per_entry, rest = u % per_entry;
-        const int seq = __ldg(p.work_list + 2 * e), t = __ldg(p.work_list + 2 * e + 1);
+        const int seq = __ldg(p.work_list + 2 * e), t0 = __ldg(p.work_list + 2 * e + 1);
         const int ql = __ldg(p.q_lens + seq), cl = __ldg(p.ctx_lens + seq), qs = __ldg(p.q_start + seq);
         U.b = seq;
-        if (p.pair_heads) {
+        int slot_tokens = kTcRows;
+        if (p.pack) {  // all heads of kv head `rest`'s group, two blocks of 128/g tokens
+            slot_tokens = kTcRows >> p.pack_shift;
+            U.hk = rest;
+            U.head[0] = U.head[1] = rest * p.g;  // first head of the group
+            U.row0[0] = t0;
+            U.row0[1] = t0 + slot_tokens;
+        } else if (p.pair_heads) {
             const int pp = rest % (p.g / 2);
             U.hk = rest / (p.g / 2);
             U.head[0] = U.hk * p.g + 2 * pp;
             U.head[1] = U.head[0] + 1;
-            U.row0[0] = U.row0[1] = t * kTcRows;
+            U.row0[0] = U.row0[1] = t0;
         } else {
             U.head[0] = U.head[1] = rest;
             U.hk = rest / p.g;
-            U.row0[0] = t * kTcRows;
-            U.row0[1] = (t + 1) * kTcRows;
+            U.row0[0] = t0;
+            U.row0[1] = t0 + kTcRows;
         }
         int last = 0;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-            U.nrows[s] = max(0, min(kTcRows, ql - U.row0[s]));
+            U.nrows[s] = max(0, min(slot_tokens, ql - U.row0[s]));  // query tokens of the slot
             U.qtok[s] = qs + U.row0[s];
             if (U.nrows[s] > 0) last = max(last, U.row0[s] + U.nrows[s]);
         }
@@ -257,13 +271,14 @@ __device__ __forceinline__ bool unit_active(const TcParams& p, const Unit& U) {
     return U.kt0 < U.n_kt;  // in masked mode [kt0, n_kt) starts and ends on a visible tile
 }
 
-// Output row r of slot s of a unit (bf16, d channels).
+// Output row of slot s of a unit (bf16, d channels): query token `tok` of the
+// slot and head sel(U.head, s) + hl (hl > 0 only for packed slots).
 template <int D, int MODE>
-__device__ __forceinline__ uint16_t* out_row(const TcParams& p, const Unit& U, int s, int r) {
+__device__ __forceinline__ uint16_t* out_row(const TcParams& p, const Unit& U, int s, int tok, int hl) {
     if constexpr (MODE == MODE_PAGED)
-        return p.out + ((long)sel(U.qtok, s) + r) * p.Hq * D + (long)sel(U.head, s) * D;
+        return p.out + ((long)sel(U.qtok, s) + tok) * p.Hq * D + (long)(sel(U.head, s) + hl) * D;
     else
-        return p.out + (((long)U.b * p.T + sel(U.row0, s) + r) * p.Hq + sel(U.head, s)) * D;
+        return p.out + (((long)U.b * p.T + sel(U.row0, s) + tok) * p.Hq + sel(U.head, s)) * D;
 }
 
 // A row that sees no key: output 0, LSE -inf (lse may be null).
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     int num_units;
     if constexpr (MODE == MODE_PAGED)
-        num_units = __ldg(p.work_count) * (p.pair_heads ? p.Hkv * (p.g / 2) : p.Hq);
+        num_units = __ldg(p.work_count) * paged_units_per_entry(p);
     else
         num_units = p.num_units;
     const int G = gridDim.x;
@@ -599,14 +614,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int u = cta_unit(sched, i, G, num_units);
             if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
-            const bool valid = r < sel(U.nrows, s);
-            const int row = sel(U.row0, s) + r;  // row within T (dense) or within the chunk (paged)
+            // query token of this thread's row, and its head within a packed slot
+            const int tok = (MODE == MODE_PAGED && p.pack) ? r >> p.pack_shift : r;
+            const int hl = (MODE == MODE_PAGED && p.pack) ? r & (p.g - 1) : 0;
+            const bool valid = tok < sel(U.nrows, s);
+            const int row = sel(U.row0, s) + tok;  // row within T (dense) or within the chunk (paged)
             if (!unit_active<MODE>(p, U)) {
                 if (valid) {
                     float* lse = nullptr;
                     if constexpr (MODE != MODE_PAGED)
                         if (p.lse) lse = p.lse + ((long)U.b * p.Hq + sel(U.head, s)) * p.T + row;
-                    store_zero_row<D>(out_row<D, MODE>(p, U, s, r), lse);
+                    store_zero_row<D>(out_row<D, MODE>(p, U, s, tok, hl), lse);
                 }
                 continue;
             }
@@ -789,7 +807,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ++oc;
             tc_fence_after();
             const Unit E = decode_unit<MODE>(p, u);  // re-derived here so its fields are not live across the tile loop
-            uint16_t* orow = out_row<D, MODE>(p, E, s, r);
+            uint16_t* orow = out_row<D, MODE>(p, E, s, tok, hl);
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             // 64 columns per TMEM wait; 32-byte stores of the bf16 row
 #pragma unroll
@@ -1011,7 +1029,10 @@ fa_status launch_paged_prefill(const void* q, const void* k_cache, const void* v
                                int total_q, cudaStream_t s, const DevCtx& ctx) {
     (void)num_seqs;
     CUtensorMap tq, tk, tv;
-    const uint32_t qbox[4] = {64, 1, (uint32_t)kTcRows, 1};
+    const int g = Hq / Hkv;
+    const bool pack = paged_tc_pack(g);
+    // packed: one box is 128/g tokens x the g heads of a group (row = token * g + head)
+    const uint32_t qbox[4] = {64, pack ? (uint32_t)g : 1u, (uint32_t)paged_tc_slot_tokens(g), 1};
     const uint64_t dq[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
     const uint64_t sq[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
     const uint32_t cbox[4] = {64, 16, 1, 1};
@@ -1022,6 +1043,8 @@ fa_status launch_paged_prefill(const void* q, const void* k_cache, const void* v
     if (st == FA_OK) st = encode_tmap_bf16_4d(&tv, v_cache, dc, scs, cbox);
     if (st != FA_OK) return st;
     TcParams p = base_params(0, 0, Hq, Hkv, causal, scale, out, nullptr, ctx);
+    p.pack = pack ? 1 : 0;
+    p.pack_shift = pack ? __builtin_ctz((unsigned)g) : 0;
     p.bt = block_table;
     p.ctx_lens = ctx_lens;
     p.q_lens = q_lens;

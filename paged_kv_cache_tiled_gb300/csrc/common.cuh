@@ -14,6 +14,23 @@
 
 namespace fa {
 
+// ------------------------------------------- paged tensor-core layout ---
+// Chunks of the paged path that go to the tensor-core kernel are cut into
+// work entries of consecutive query tokens; each entry is one unit per kv
+// head (or per pair of query heads), two 128-row Q slots sharing every K/V
+// tile.  When the GQA group size g = Hq/Hkv divides 128 (g = 2, 4, 8, 16) a
+// slot packs 128/g tokens x the g heads of the group (row = token * g + head),
+// so a short chunk does not pad a 128-row tile per head; otherwise a slot is
+// 128 tokens of one head.
+__host__ __device__ inline bool paged_tc_pack(int g) { return g == 2 || g == 4 || g == 8 || g == 16; }
+// tokens of a query slot
+__host__ __device__ inline int paged_tc_slot_tokens(int g) { return paged_tc_pack(g) ? 128 / g : 128; }
+// query tokens of a work entry: two packed slots; a head pair's two slots over
+// the same 128 tokens (g even); or two consecutive 128-token slots of one head
+__host__ __device__ inline int paged_tc_entry_tokens(int g) {
+    return paged_tc_pack(g) ? 2 * (128 / g) : (g % 2 == 0 ? 128 : 256);
+}
+
 // ---------------------------------------------------------------- errors ---
 // Bits of the per-device error word.
 enum : unsigned { ERR_BOUNDS_BIT = 1u, ERR_TIMEOUT_BIT = 2u };

@@ -63,7 +63,7 @@ inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, i
     (void)Hkv;
     (void)mbps;
     PagedWs w{};
-    w.max_entries = total_q / 128 + num_seqs + 1;
+    w.max_entries = total_q / 16 + num_seqs + 1;  // entries hold at least 16 tokens (paged_tc_entry_tokens)
     size_t off = 0;
     w.q_start = off;
     off = align256(off + sizeof(int32_t) * (size_t)(num_seqs + 1));
@@ -695,13 +695,14 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
 }
 
 // ------------------------------------------------------------ metadata -----
-// One CTA: q_start (exclusive prefix sum of q_lens) and the list of query
-// tiles (or tile pairs) of the sequences that take the tensor-core kernel,
-// ordered by decreasing number of KV tiles (longest first) with a counting
-// sort.  Entry = (sequence, first 128-row tile).
+// One CTA: q_start (exclusive prefix sum of q_lens) and the list of work
+// entries (entry_tokens consecutive query tokens, paged_tc_entry_tokens) of
+// the sequences that take the tensor-core kernel, ordered by decreasing number
+// of KV tiles (longest first) with a counting sort.  Entry = (sequence, first
+// query token of the entry within the chunk).
 __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restrict__ ctx_lens,
                                                           const int32_t* __restrict__ q_lens, int num_seqs, int mbps,
-                                                          int g, int causal, int tiles_per_entry,
+                                                          int g, int causal, int entry_tokens,
                                                           int32_t* __restrict__ q_start, int32_t* __restrict__ count,
                                                           int32_t* __restrict__ list, int max_entries,
                                                           DevCtx ctx) {
@@ -744,7 +745,7 @@ __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restr
     if (threadIdx.x == 0) q_start[num_seqs] = carry;
     // histogram of entry costs
     auto entry_cost = [&](int ql, int cl, int t0) {
-        const int last_row = min(ql, t0 + 128 * tiles_per_entry) - 1;  // last query row of the entry
+        const int last_row = min(ql, t0 + entry_tokens) - 1;  // last query row of the entry
         const int kv_end = causal ? cl - ql + last_row + 1 : cl;
         return (kv_end + 127) / 128;
     };
@@ -755,8 +756,7 @@ __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restr
             raise_error(ctx, ERR_BOUNDS_BIT);
             continue;
         }
-        const int ntile = (ql + 127) / 128;
-        for (int t = 0; t < ntile; t += tiles_per_entry) atomicAdd(&hist[entry_cost(ql, cl, t * 128)], 1);
+        for (int t0 = 0; t0 < ql; t0 += entry_tokens) atomicAdd(&hist[entry_cost(ql, cl, t0)], 1);
     }
     __syncthreads();
     if (threadIdx.x == 0) {  // bucket starts, highest cost first
@@ -773,12 +773,11 @@ __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restr
     for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
         const int ql = q_lens[s], cl = ctx_lens[s];
         if (ql <= 0 || is_decode_row(ql, g) || ql > cl || cl > mbps * kBS) continue;
-        const int ntile = (ql + 127) / 128;
-        for (int t = 0; t < ntile; t += tiles_per_entry) {
-            const int pos = atomicAdd(&hist[entry_cost(ql, cl, t * 128)], 1);
+        for (int t0 = 0; t0 < ql; t0 += entry_tokens) {
+            const int pos = atomicAdd(&hist[entry_cost(ql, cl, t0)], 1);
             if (pos < max_entries) {
                 list[2 * pos] = s;
-                list[2 * pos + 1] = t;
+                list[2 * pos + 1] = t0;
             }
         }
     }
@@ -889,7 +888,7 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
         if (st != FA_OK) return st;
     }
     if (!is_decode_row(max_q_len, g)) {
-        const int tiles_per_entry = (g % 2 == 0) ? 1 : 2;
+        const int entry_tokens = paged_tc_entry_tokens(g);
         int32_t* q_start = reinterpret_cast<int32_t*>(wsb + w.q_start);
         int32_t* count = reinterpret_cast<int32_t*>(wsb + w.work_count);
         int32_t* list = reinterpret_cast<int32_t*>(wsb + w.work_list);
@@ -900,7 +899,7 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
             (st = raise_dynamic_smem(reinterpret_cast<const void*>(paged_meta_kernel), (int)hist_bytes)) != FA_OK)
             return st;
         paged_meta_kernel<<<1, 1024, hist_bytes, s>>>(ctx_lens, q_lens, num_seqs, max_blocks_per_seq, g, causal,
-                                                      tiles_per_entry, q_start, count, list, w.max_entries, ctx);
+                                                      entry_tokens, q_start, count, list, w.max_entries, ctx);
         if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
         ++launches;
         st = launch_paged_prefill(q, k_cache, v_cache, block_table, ctx_lens, q_lens, q_start, list, count, out,

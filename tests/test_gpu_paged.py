@@ -108,6 +108,10 @@ MIXED = [
     ([0, 200, 63, 1], [129, 130, 1, 2], 6, 2, 128),                              # g = 3 (odd): tile pairs
     ([10, 3000, 0, 257], [1, 1, 256, 33], 4, 4, 64),                             # MHA, d = 64
     ([4095, 1, 17], [1, 513, 127], 12, 2, 128),                                  # g = 6, long chunk
+    # packed query slots (128/g tokens x the g heads of a group per 128-row tile)
+    ([100, 0, 7], [200, 9, 64], 4, 2, 64),                                       # g = 2, d = 64
+    ([2000, 17, 0], [129, 64, 31], 16, 2, 128),                                  # g = 8
+    ([0, 900, 33, 5], [70, 5, 300, 2], 16, 1, 128),                              # g = 16: 8 tokens per slot
 ]
 
 
