@@ -189,8 +189,9 @@ fa_status fa_cache_append_rope(const void* q, const void* k, const void* v, cons
 
 /*
  * fa_cache_append_fp8 / fa_paged_attn_fp8 -- the 8-bit (E4M3) KV cache.
- * Passage: "Further Reading" cites 8-bit matrix arithmetic ("8-bit MMA");
- * the pages fix no format or scale convention.  Reading: E4M3 (1 sign, 4
+ * Passage: page 3, "Key Details" (the fused kernels use the GPU's 16-bit or
+ * 8-bit matrix-multiply-accumulate units); the pages fix no format or scale
+ * convention.  Reading: E4M3 (1 sign, 4
  * exponent bits, bias 7, 3 mantissa bits, largest finite 448, S.1111.111 NaN),
  * one scale per cache: code = E4M3(x / scale), division in binary32, round to
  * nearest even, saturating at +-448; the cached value is E4M3 * scale.
