@@ -90,10 +90,14 @@ fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int
  *   q, k, v, out            device buffers of the same shapes, with
  *                           fa_prefill's alignment rules; the caller owns them
  *                           and they are overwritten (q, k, v with the inputs)
- * The batch is processed one sequence at a time: while sequence b is computed
- * on `stream`, the inputs of b+1 are copied in and the output of b-1 is copied
- * out on two library-owned streams, so copies in both directions overlap the
- * kernels.  The output equals fa_prefill's for the whole batch bit for bit.
+ * The key and value rows are copied in first, then the query rows in row
+ * chunks (rows [c*R, (c+1)*R) of every sequence, R = max(128, T/4 rounded up
+ * to a multiple of 128)) from the last chunk to the first, on a
+ * library-owned stream; each chunk's attention runs on `stream` as soon as
+ * its query rows are in, and its output is copied out on a second
+ * library-owned stream, so copies in both directions overlap the kernels.
+ * One launch per chunk.  The output equals fa_prefill's for the whole batch
+ * bit for bit.
  * Ordered on `stream` like any other call: it starts after the work already
  * queued there, and work queued after it sees out_host written; the host is
  * not synchronised.  No LSE output.  Errors: as fa_prefill, plus

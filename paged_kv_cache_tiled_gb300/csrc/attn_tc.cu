@@ -68,7 +68,9 @@ struct TcCfg {
 };
 
 struct TcParams {
-    int B, T;        // dense / masked: Tq = Tk = T
+    int B, T;        // dense / masked: sequence length (row stride of q/k/v/out)
+    int q0, Tq, Tk;  // dense: query rows [q0, q0 + Tq) of each sequence against keys [0, Tk)
+                     // (q0 a multiple of 128; q0 = 0, Tq = Tk = T for the whole problem)
     int Hq, Hkv, g;
     int causal;
     float scale_log2;
@@ -189,7 +191,8 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
         U.kt0 = 0;
         U.n_kt = (kv_end + kTcRows - 1) / kTcRows;
     } else {
-        const int nqt = (p.T + kTcRows - 1) / kTcRows;
+        const int nqt = (p.Tq + kTcRows - 1) / kTcRows;  // query tiles of this launch
+        const int qt0 = p.q0 / kTcRows;                  // its first tile within the sequence
         if (p.pair_heads) {
             const int half = p.g / 2;
             const int upt = p.B * p.Hkv * half;
@@ -204,7 +207,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
             const int pp = rest % half;
             U.head[0] = U.hk * p.g + 2 * pp;
             U.head[1] = U.head[0] + 1;
-            U.row0[0] = U.row0[1] = qt * kTcRows;
+            U.row0[0] = U.row0[1] = (qt0 + qt) * kTcRows;
         } else {
             const int ntp = (nqt + 1) / 2;
             const int upt = p.B * p.Hq;
@@ -213,19 +216,19 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
             U.b = rest / p.Hq;
             U.head[0] = U.head[1] = rest % p.Hq;
             U.hk = U.head[0] / p.g;
-            U.row0[0] = 2 * pt * kTcRows;
-            U.row0[1] = (2 * pt + 1) * kTcRows;
+            U.row0[0] = (qt0 + 2 * pt) * kTcRows;
+            U.row0[1] = (qt0 + 2 * pt + 1) * kTcRows;
         }
         int last = 0;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-            U.nrows[s] = max(0, min(kTcRows, p.T - U.row0[s]));
+            U.nrows[s] = max(0, min(kTcRows, p.q0 + p.Tq - U.row0[s]));
             U.qtok[s] = U.row0[s];
             if (U.nrows[s] > 0) last = max(last, U.row0[s] + U.nrows[s]);
         }
-        U.kv_len = p.T;
-        U.pos_off = 0;
-        const int kv_end = p.causal ? last : p.T;
+        U.kv_len = p.Tk;
+        U.pos_off = 0;  // rows and keys are both absolute positions in the sequence
+        const int kv_end = p.causal ? min(p.Tk, last) : p.Tk;
         U.kt0 = 0;
         U.n_kt = (kv_end + kTcRows - 1) / kTcRows;
         if constexpr (MODE == MODE_MASKED) {
@@ -896,6 +899,7 @@ static fa_status launch_tc_d(int d, const CUtensorMap& tq, const CUtensorMap& tk
 // Cached per (B, T, Hq, Hkv, grid): the result depends on nothing else.
 static const TcSched* dense_schedule(const TcParams& p, int grid) {
     if (!p.causal || p.num_units > kMaxSchedUnits || grid > kMaxSchedCtas || grid <= 0) return nullptr;
+    if (p.q0 != 0 || p.Tq != p.T || p.Tk != p.T) return nullptr;  // row windows take the dealt order
     struct Key {
         int B, T, Hq, Hkv, grid;
         bool operator==(const Key& o) const {
@@ -1005,6 +1009,9 @@ static TcParams base_params(int B, int T, int Hq, int Hkv, int causal, float sca
     TcParams p{};
     p.B = B;
     p.T = T;
+    p.q0 = 0;
+    p.Tq = T;
+    p.Tk = T;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.g = Hq / Hkv;
@@ -1018,7 +1025,7 @@ static TcParams base_params(int B, int T, int Hq, int Hkv, int causal, float sca
 }
 
 static int dense_units(const TcParams& p) {
-    const int nqt = (p.T + kTcRows - 1) / kTcRows;
+    const int nqt = (p.Tq + kTcRows - 1) / kTcRows;
     return p.pair_heads ? p.B * p.Hkv * (p.g / 2) * nqt : p.B * p.Hq * ((nqt + 1) / 2);
 }
 
@@ -1054,6 +1061,28 @@ fa_status launch_paged_prefill(const void* q, const void* k_cache, const void* v
     p.mbps = mbps;
     p.num_blocks = num_blocks;
     return launch_tc_d<MODE_PAGED>(d, tq, tk, tv, p, sm_count(), s);
+}
+
+// Query rows [q0, q0 + Tq) of every sequence against keys [0, Tk), for the
+// host pipeline: arguments as fa_prefill's (already checked by the caller),
+// q0 a multiple of 128, q0 + Tq <= T, Tk <= T.  The rows computed here are bit
+// for bit those of the whole-problem call: the same query tiles meet the same
+// key tiles in the same order.
+fa_status launch_prefill_rows(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                              int d, int causal, float scale, int q0, int Tq, int Tk, cudaStream_t s) {
+    if (q0 < 0 || (q0 % kTcRows) != 0 || Tq <= 0 || q0 + Tq > T || Tk <= 0 || Tk > T) return FA_ERR_INVALID_ARG;
+    DevCtx ctx;
+    fa_status st = make_ctx(&ctx);
+    if (st != FA_OK) return st;
+    CUtensorMap tq, tk, tv;
+    if ((st = dense_maps(q, k, v, B, T, Hq, Hkv, d, &tq, &tk, &tv)) != FA_OK) return st;
+    TcParams p = base_params(B, T, Hq, Hkv, causal, scale, out, nullptr, ctx);
+    p.q0 = q0;
+    p.Tq = Tq;
+    p.Tk = Tk;
+    p.num_units = dense_units(p);
+    const int grid = std::min(p.num_units, sm_count());
+    return launch_tc_d<MODE_DENSE>(d, tq, tk, tv, p, grid, s, dense_schedule(p, grid));
 }
 
 }  // namespace fa

@@ -36,6 +36,11 @@ fa_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t
 fa_status encode_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
                          const uint32_t box[4], CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle);
 
+// Prefill of query rows [q0, q0 + Tq) of every sequence against keys [0, Tk)
+// (defined in attn_tc.cu; used by the host-buffer pipeline).
+fa_status launch_prefill_rows(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                              int d, int causal, float scale, int q0, int Tq, int Tk, cudaStream_t s);
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

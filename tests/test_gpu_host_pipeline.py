@@ -1,7 +1,9 @@
-"""Prefill from and to host memory (fa_prefill_host): the pipelined copies give
-exactly fa_prefill's output (bit for bit, since each sequence's work units are
-the same), which is itself checked against the fp64 oracle here too; pinned
-and pageable host memory, d in {64, 128}, causal and not, ragged T, a
+"""Prefill from and to host memory (fa_prefill_host): the copies and the
+attention are pipelined over row chunks of the batch (last rows first), and the result is
+exactly fa_prefill's output (bit for bit: each chunk's launch meets the same
+query tiles with the same key tiles in the same order), which is itself
+checked against the fp64 oracle here too; pinned and pageable host memory, d
+in {64, 128}, causal and not, ragged T, several chunks per sequence, a
 non-default stream, and buffers reused across calls."""
 import numpy as np
 import pytest
@@ -35,7 +37,9 @@ def host_copies(case, pinned):
     (3, 300, 4, 2, 128, True, True),     # ragged final tile, GQA 2
     (2, 129, 6, 2, 64, False, False),    # d = 64, non-causal, pageable host memory
     (4, 256, 12, 2, 128, True, True),    # GQA 6 (odd pairs), whole tiles
-    (1, 77, 2, 2, 128, True, True),      # a single sequence (no overlap to gain)
+    (1, 77, 2, 2, 128, True, True),      # a single sequence, a single chunk
+    (2, 2048, 12, 2, 128, True, True),   # four 512-row chunks (config 2's row split)
+    (2, 1100, 4, 1, 64, False, True),    # non-causal, several chunks
 ])
 def test_host_pipeline_matches_device_path(F, B, T, Hq, Hkv, d, causal, pinned):
     case = W.prefill_case(31 + B, B, T, Hq, Hkv, d, causal)
@@ -45,7 +49,8 @@ def test_host_pipeline_matches_device_path(F, B, T, Hq, Hkv, d, causal, pinned):
     F.fa_prefill_host(hq, hk, hv, hout, q, k, v, out, causal=causal, scale=case.scale)
     torch.cuda.synchronize()
     assert F.fa_get_error() == F.FA_OK
-    assert F.fa_last_launch_count() == B
+    rows = max(128, (T // 4 + 127) // 128 * 128)
+    assert F.fa_last_launch_count() == (T + rows - 1) // rows  # one launch per row chunk
     # the device buffers hold the inputs and the output afterwards
     for dev, host in ((q, hq), (k, hk), (v, hv), (out, hout)):
         assert torch.equal(dev.cpu(), host)
