@@ -629,7 +629,7 @@ def main():
         r4 = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks, masked=True)
         r4c = bench_prefill(F, timer, c4, steps4, min(args.warmup, 3), ws, peaks, causal=True)
         tc_sus = float(peaks.get("bf16_tflops_sustained", tc_peak))
-        for r, name, tkey in ((r4, "additive mask M (-inf above diagonal) via fa_prefill_masked", None),
+        for r, name, tkey in ((r4, "additive mask M (-inf above diagonal) via fa_prefill_masked", "attn_tc_masked_c4"),
                               (r4c, "causal flag via fa_prefill", "attn_tc_dense_c4")):
             sec.append({"workload": f"config 4: long prefill B=1 T=16384 Hq=32 Hkv=8 d=128, {name}",
                         "metric": "prefill attn TFLOP/s", "value": r["tflops"], "unit": "TFLOP/s",
@@ -654,7 +654,7 @@ def main():
                     "gpu_launches": ml, "algorithmic_bytes": mbytes,
                     "roofline": {"bound": "hbm", "achieved": mgbs, "peak": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
                                  "unit": "GB/s", "frac": mgbs / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
-                                 "traffic": None, "peak_source": f"{peak_src} hbm copy",
+                                 "traffic": traffic.get("mask_classify_c4"), "peak_source": f"{peak_src} hbm copy",
                                  "kernel": "mask_classify_kernel"}})
         del c4, r4, r4c, M4, cls4
         torch.cuda.empty_cache()
