@@ -297,6 +297,30 @@ def paged_flops(p):
     return tot
 
 
+def paged_issued_flops(p):
+    """MMA work the chunked-prefill launch issues for the chunks that take the
+    tensor-core path (whole 128x128 score tiles for both products), next to the
+    decode rows' algorithmic work: each work entry covers 2*128/g tokens of one
+    kv head when g = Hq/Hkv divides 128 (packed tiles), else 128 tokens of a
+    head pair or 256 tokens of one head; it scans the 128-key tiles up to its
+    last token's position."""
+    g = p.Hq // p.Hkv
+    pack = g in (2, 4, 8, 16)
+    ent = 2 * (128 // g) if pack else (128 if g % 2 == 0 else 256)
+    per_entry_rows = 2 * 128  # two 128-row slots per unit
+    units_per_entry = p.Hkv if pack else (p.Hkv * (g // 2) if g % 2 == 0 else p.Hq)
+    tot = 0.0
+    for c, q in zip(p.ctx_lens.numpy().astype(np.int64), p.q_lens.numpy().astype(np.int64)):
+        if q * g <= 16:
+            tot += W.attention_flops(int(q), int(c), p.d, p.Hq, p.causal)
+            continue
+        for t0 in range(0, int(q), ent):
+            last = min(int(q), t0 + ent)
+            n_kt = -(-(int(c) - int(q) + last) // 128) if p.causal else -(-int(c) // 128)
+            tot += units_per_entry * n_kt * 4.0 * per_entry_rows * 128 * p.d
+    return tot
+
+
 def bench_paged(F, timer, p, steps, warmup, ws, with_append=False):
     t = paged_setup(F, p)
     max_q = int(p.q_lens.max())
@@ -669,6 +693,7 @@ def main():
                                 "Hq=32 Hkv=8 d=128",
                     "metric": "prefill attn TFLOP/s", "value": tf5, "unit": "TFLOP/s", "ms_per_step": r5["ms"],
                     "gpu_launches": r5["launches"], "algorithmic_flops": f5, "algorithmic_bytes": b5,
+                    "issued_over_algorithmic_flops": paged_issued_flops(c5) / f5,
                     "roofline": {"bound": "tensor" if f5 / (tc_peak * 1e12) > b5 / (hbm * 1e9) else "hbm",
                                  "achieved": tf5, "peak": tc_peak, "unit": "TFLOP/s",
                                  "frac": t_bound / (r5["ms"] * 1e-3), "traffic": traffic.get("attn_tc_paged_c5"),
