@@ -47,6 +47,7 @@
 namespace fa {
 
 enum { MODE_DENSE = 0, MODE_MASKED = 1, MODE_PAGED = 2 };
+constexpr int kRangeHoles = 1 << 30;  // flag bit of a query tile's visible KV range
 constexpr int kTcThreads = 320;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kTcRows = 128;  // rows of a Q tile and of a KV tile
@@ -84,7 +85,8 @@ struct TcParams {
     const float* mask;
     const uint8_t* cls;
     const int32_t* qt_order;
-    const int2* qt_range;  // per query tile: [first, last+1) of its KV tiles that are not all -inf
+    const int2* qt_range;  // per query tile: [first, last+1) of its KV tiles that are not all -inf;
+                           // kRangeHoles set in .x when an all -inf tile lies inside that range
     // paged
     const int32_t* bt;
     const int32_t* ctx_lens;
@@ -107,6 +109,7 @@ struct Unit {
     int pos_off;    // key position of query row i is i + pos_off
     int kt0;        // first KV tile to scan
     int n_kt;       // KV tiles to scan: [kt0, n_kt)
+    int holes;      // masked: some tile in [kt0, n_kt) is all -inf for both slots (must be skipped)
 };
 
 // Per-slot field of a unit.  A select instead of a runtime array index keeps
@@ -153,6 +156,7 @@ __device__ __forceinline__ int paged_units_per_entry(const TcParams& p) {
 template <int MODE>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
     Unit U;
+    U.holes = 0;
     if constexpr (MODE == MODE_PAGED) {
         const int per_entry = paged_units_per_entry(p);
         const int e = u / per_entry, rest = u % per_entry;
@@ -232,15 +236,24 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
         U.kt0 = 0;
         U.n_kt = (kv_end + kTcRows - 1) / kTcRows;
         if constexpr (MODE == MODE_MASKED) {
-            // restrict the scan to the KV tiles the mask leaves visible
-            int lo = U.n_kt, hi = 0;
+            // restrict the scan to the KV tiles the mask leaves visible; the
+            // tiles inside that range need a per-tile class check only when
+            // one of them is all -inf for both slots (a hole in a slot's range,
+            // or a gap between the two slots' ranges)
+            int lo = U.n_kt, hi = 0, lo_s[2] = {0, 0}, hi_s[2] = {0, 0}, live = 0;
 #pragma unroll
             for (int s = 0; s < 2; ++s)
                 if (U.nrows[s] > 0) {
                     const int2 r = __ldg(p.qt_range + U.row0[s] / kTcRows);
-                    lo = min(lo, r.x);
+                    const int rlo = r.x & (kRangeHoles - 1);
+                    lo_s[s] = rlo;
+                    hi_s[s] = r.y;
+                    lo = min(lo, rlo);
                     hi = max(hi, r.y);
+                    U.holes |= (r.x & kRangeHoles) ? 1 : 0;
+                    ++live;
                 }
+            if (live == 2 && (hi_s[0] < lo_s[1] || hi_s[1] < lo_s[0])) U.holes = 1;
             U.kt0 = lo;
             U.n_kt = min(U.n_kt, hi);
         }
@@ -263,7 +276,7 @@ __device__ __forceinline__ int tile_class(const TcParams& p, const Unit& U, int 
 template <int MODE>
 __device__ __forceinline__ bool skip_tile(const TcParams& p, const Unit& U, int kt) {
     if constexpr (MODE == MODE_MASKED)
-        return tile_class<MODE>(p, U, 0, kt) == 0 && tile_class<MODE>(p, U, 1, kt) == 0;
+        return U.holes && tile_class<MODE>(p, U, 0, kt) == 0 && tile_class<MODE>(p, U, 1, kt) == 0;
     else
         return false;
 }
@@ -860,7 +873,8 @@ __global__ void __launch_bounds__(256) mask_order_kernel(const uint8_t* __restri
                 hi = k + 1;
             }
         cost[q] = c;
-        range[q] = make_int2(lo, hi);
+        // flag: an all -inf tile inside [lo, hi) (the scan must check classes)
+        range[q] = make_int2(lo | (c > 0 && c < hi - lo ? kRangeHoles : 0), hi);
     }
     __syncthreads();
     for (int q = threadIdx.x; q < nqt; q += blockDim.x) {
