@@ -379,6 +379,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ================================================== TMA producer ====
         int fill = 0, qcnt = 0;
         bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
+        // At kernel start every CTA requests its first Q tiles and its first
+        // K/V tiles at once; the rest of the ring waits until the Q tiles are
+        // in, so that the first Q K^T is not queued behind the whole ring's
+        // copies of every CTA.
+        bool held = true;
         for (int i = 0; ok; ++i) {
             const int u = cta_unit(sched, i, G, num_units);
             if (u < 0) break;
@@ -406,6 +411,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ++qcnt;
             for (int kt = U.kt0; kt < U.n_kt && ok; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
+                if (held && fill == 2) {  // first K/V pair issued: let this unit's Q tiles land
+                    held = false;
+                    for (int s2 = 0; s2 < 2 && ok; ++s2)
+                        if (!mbar_wait_warp(&qfull[s2], (qcnt - 1) & 1, lim_ns, abort_flag)) ok = false;
+                    if (!ok) break;
+                }
                 for (int which = 0; which < 2; ++which) {  // 0: K tile, 1: V tile
                     const int stage = fill % S;
                     if (!mbar_wait_warp(&empty[stage], ((fill / S) & 1) ^ 1, lim_ns, abort_flag)) {
