@@ -81,6 +81,27 @@ fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int
                      fa_stream_t stream);
 
 /*
+ * fa_prefill_rows -- fa_prefill for a window of query rows: rows
+ * [q0, q0 + Tq) of every sequence against keys [0, Tk) (a chunk of a longer
+ * prefill whose keys and values are already in place).
+ * Passage: "FlashAttention-Style Kernels" (each query tile is combined with
+ * the key tiles it can see; the causal mask keeps key j for query i when
+ * j <= i, positions counted from the start of the sequence).
+ *   q, k, v, out, B, T, Hq, Hkv, d, causal, scale: as fa_prefill (the buffers
+ *       hold whole sequences; only rows [q0, q0 + Tq) of q and out, and rows
+ *       [0, Tk) of k and v, are read or written)
+ *   q0  a multiple of 128; 0 <= q0, q0 + Tq <= T
+ *   Tk  1 <= Tk <= T; with causal != 0, Tk >= q0 + Tq (every key a row can see)
+ * The rows written equal, bit for bit, the same rows of fa_prefill over the
+ * whole problem when Tk covers them (the same query tiles meet the same key
+ * tiles in the same order).  FA_ERR_INVALID_ARG for a window outside those
+ * bounds; other errors as fa_prefill.
+ */
+fa_status fa_prefill_rows(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,
+                          int Hkv, int d, int causal, float scale, int q0, int Tq, int Tk,
+                          fa_stream_t stream);
+
+/*
  * fa_prefill_host -- fa_prefill with the inputs and the output in host memory.
  * Passage: "FlashAttention-Style Kernels" (same computation as fa_prefill);
  * the copies are the runtime around it.

@@ -1135,6 +1135,20 @@ fa_status fa_prefill(const void* q, const void* k, const void* v, void* out, int
     return st;
 }
 
+fa_status fa_prefill_rows(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                          int d, int causal, float scale, int q0, int Tq, int Tk, fa_stream_t stream) {
+    set_launch_count(0);
+    fa_status st = check_prefill_args(q, k, v, out, B, T, Hq, Hkv, d, scale);
+    if (st != FA_OK || B == 0 || T == 0 || Tq == 0) return st;
+    if (q0 < 0 || (q0 % kTcRows) != 0 || Tq < 0 || q0 + Tq > T || Tk <= 0 || Tk > T || (causal && Tk < q0 + Tq))
+        return FA_ERR_INVALID_ARG;
+    if ((st = check_device()) != FA_OK) return st;
+    st = launch_prefill_rows(q, k, v, out, B, T, Hq, Hkv, d, causal, scale, q0, Tq, Tk,
+                             reinterpret_cast<cudaStream_t>(stream));
+    if (st == FA_OK) set_launch_count(1);
+    return st;
+}
+
 size_t fa_prefill_masked_workspace_size(int T) {
     if (T <= 0) return 0;
     const size_t nt = (size_t)(T + kTcRows - 1) / kTcRows;

@@ -31,6 +31,7 @@ EXPORTS = [
     "fa_decode_graph_destroy", "fa_pool_create", "fa_pool_destroy", "fa_pool_add_seq", "fa_pool_fork",
     "fa_pool_append", "fa_pool_release", "fa_pool_tables", "fa_pool_num_free", "fa_pool_refcount", "fa_pool_seq_len",
     "fa_copy_blocks", "fa_cache_append_fp8", "fa_paged_attn_fp8", "fa_prefill_host", "fa_mask_tile_classes",
+    "fa_prefill_rows",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20  # FA_NOALLOC_SCRATCH_BYTES
 
@@ -51,6 +52,7 @@ def _load() -> ctypes.CDLL:
         "fa_status_string": (ctypes.c_char_p, [I]),
         "fa_prefill": (I, [P, P, P, P, I, I, I, I, I, I, F, P, P]),
         "fa_prefill_host": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]),
+        "fa_prefill_rows": (I, [P, P, P, P, I, I, I, I, I, I, F, I, I, I, P]),
         "fa_prefill_masked_workspace_size": (Z, [I]),
         "fa_prefill_masked": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, Z, P]),
         "fa_stage_bf16": (I, [P, P, Z, P]),
@@ -148,6 +150,24 @@ def fa_prefill(q, k, v, causal: bool = True, scale: float | None = None, out=Non
         _need(lse, "lse", torch.float32)
     _check(_lib.fa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, d, int(causal), float(scale),
                            _ptr(lse), _stream(stream)), "fa_prefill")
+    return out
+
+
+def fa_prefill_rows(q, k, v, q0: int, Tq: int, Tk: int, causal: bool = True, scale: float | None = None, out=None,
+                    stream=None):
+    """Query rows [q0, q0+Tq) of every sequence against keys [0, Tk); q/k/v/out
+    hold whole sequences [B, T, H, d] and only those rows of `out` are written."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, torch.bfloat16, 4)
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4)
+    _check(_lib.fa_prefill_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, d, int(causal), float(scale),
+                                int(q0), int(Tq), int(Tk), _stream(stream)), "fa_prefill_rows")
     return out
 
 

@@ -126,3 +126,38 @@ def test_config4_full_size_sampled(F):
     ref, _ = oracle.attention_rows(case.q, case.k, case.v, False, case.scale, rows, mask=case.mask)
     got = out_m[0, rows[:, 2], rows[:, 1]]
     assert_parity(got, ref, "c4 sampled")
+
+
+@pytest.mark.parametrize("q0,Tq,Tk,causal", [(0, 300, 300, True), (128, 200, 600, True), (256, 77, 333, True),
+                                              (384, 216, 600, True), (128, 100, 250, False), (0, 600, 37, False)])
+def test_prefill_rows_window(F, q0, Tq, Tk, causal):
+    """A window of query rows against the first Tk keys: the oracle on the
+    window (causal positions counted from the start of the sequence), the rows
+    of the whole-problem call bit for bit, and nothing outside the window
+    written."""
+    case = W.prefill_case(51, 2, 600, 6, 2, 128, causal)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    out = torch.full_like(q, 3.0)
+    F.fa_prefill_rows(q, k, v, q0, Tq, Tk, causal=causal, scale=case.scale, out=out)
+    assert F.fa_get_error() == F.FA_OK
+    assert torch.all(out[:, :q0] == 3.0) and torch.all(out[:, q0 + Tq:] == 3.0)
+    win = out[:, q0:q0 + Tq]
+    if causal:
+        full = F.fa_prefill(q, k, v, causal=True, scale=case.scale)
+        assert torch.equal(win, full[:, q0:q0 + Tq])
+        kend = q0 + Tq  # keys past the last row are masked anyway; bottom-right alignment puts row i at q0 + i
+    else:
+        kend = Tk
+    ref, _ = oracle.attention(case.q[:, q0:q0 + Tq].contiguous(), case.k[:, :kend].contiguous(),
+                              case.v[:, :kend].contiguous(), causal, case.scale)
+    assert_parity(win, ref, f"rows [{q0}, {q0 + Tq}) against {Tk} keys")
+
+
+def test_prefill_rows_rejects_bad_windows(F):
+    case = W.prefill_case(52, 1, 256, 2, 1, 64, True)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    for q0, Tq, Tk, causal in ((64, 10, 256, True),     # q0 not a multiple of 128
+                               (128, 200, 256, True),   # past the sequence
+                               (0, 200, 100, True)):    # causal rows that see keys past Tk
+        with pytest.raises(F.FattnError):
+            F.fa_prefill_rows(q, k, v, q0, Tq, Tk, causal=causal, scale=case.scale)
