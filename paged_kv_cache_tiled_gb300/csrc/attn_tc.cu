@@ -304,6 +304,42 @@ __device__ __noinline__ void store_zero_row(uint16_t* orow, float* lse) {
     if (lse) *lse = -INFINITY;
 }
 
+// Zeroes rows [z0, z1) of a staged K/V tile (both 64-channel atoms; every
+// 16-byte chunk of a row, so the swizzle does not matter) and makes the writes
+// visible to the tensor core.  Called by a whole warp.  Kept out of line: the
+// call is rare (the last, partly filled block of a context), and inlined into
+// the MMA issue loop it slowed that loop by about 10 %.
+template <int D>
+__device__ __noinline__ void zero_tile_rows(uint8_t* base, int z0, int z1) {
+    using C = TcCfg<D>;
+    const int n16 = (z1 - z0) * C::kAtoms * 8;
+    for (int e = threadIdx.x & 31; e < n16; e += 32) {
+        const int row = z0 + e / (C::kAtoms * 8);
+        const int a = (e / 8) % C::kAtoms;
+        *reinterpret_cast<uint4*>(base + a * C::kAtomBytes + row * 128 + (e % 8) * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
+// Multiplies this thread's TMEM row of D fp32 columns at taddr by alpha (the
+// in-place rescale of O when the running max has grown).  Out of line: it is
+// rare after the first tiles, and inlined into the softmax loop it cost about
+// 3 % on short prefills.
+template <int D>
+__device__ __noinline__ void scale_tmem_row(uint32_t taddr, float alpha) {
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(taddr + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+        tmem_st32(taddr + c * 32, o);
+    }
+    tmem_wait_st();
+}
+
 // ------------------------------------------------------------------ kernel --
 template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -485,18 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int kv0 = vkt * kTcRows;
                 const int z0 = kv_len - kv0;
                 const int z1 = min(kTcRows, ((kv_len + 15) & ~15) - kv0);
-                if (z0 < z1) {
-                    uint8_t* base = ring + (vidx % S) * C::kTileBytes;
-                    const int n16 = (z1 - z0) * C::kAtoms * 8;
-                    for (int e = lane; e < n16; e += 32) {
-                        const int row = z0 + e / (C::kAtoms * 8);
-                        const int a = (e / 8) % C::kAtoms;
-                        *reinterpret_cast<uint4*>(base + a * C::kAtomBytes + row * 128 + (e % 8) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
+                if (z0 < z1) zero_tile_rows<D>(ring + (vidx % S) * C::kTileBytes, z0, z1);
             }
             return true;
         };
@@ -810,16 +835,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 l += ((rsp[0].x + rsp[0].y) + (rsp[1].x + rsp[1].y)) + ((rsp[2].x + rsp[2].y) + (rsp[3].x + rsp[3].y));
                 if (rescale_o) {
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(trow + o_col + c * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                        tmem_st32(trow + o_col + c * 32, o);
-                    }
-                    tmem_wait_st();
+                    scale_tmem_row<D>(trow + o_col, alpha);
                     tc_fence_before();
                     mbar_arrive(&pfull[2 * s]);
                     mbar_arrive(&pfull[2 * s + 1]);
