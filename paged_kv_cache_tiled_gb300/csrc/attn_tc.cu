@@ -445,8 +445,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (!ok) break;
             ++qcnt;
+            // paged: lanes 0-15 each copy one 16-token block (lane & 7) of one
+            // 64-channel half; the block-table entry of the next tile is read a
+            // tile ahead, so its load latency is off the copy path
+            auto load_blk = [&](int kt) -> int {
+                const int lb = kt * 8 + (lane & 7);
+                return (lane < 8 * C::kAtoms && lb * 16 < U.kv_len) ? __ldg(p.bt + (long)U.b * p.mbps + lb) : 0;
+            };
+            int blk_next = 0;
+            if constexpr (MODE == MODE_PAGED) blk_next = load_blk(U.kt0);
             for (int kt = U.kt0; kt < U.n_kt && ok; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
+                int blk = p.num_blocks;  // outside the map: the copy fills zeros
+                if constexpr (MODE == MODE_PAGED) {
+                    const int cur = blk_next;
+                    if (kt + 1 < U.n_kt) blk_next = load_blk(kt + 1);
+                    if (lane < 8 * C::kAtoms && (kt * 8 + (lane & 7)) * 16 < U.kv_len) {
+                        if (cur < 0 || cur >= p.num_blocks)
+                            raise_error(p.ctx, ERR_BOUNDS_BIT);
+                        else
+                            blk = cur;
+                    }
+                }
                 if (held && fill == 2) {  // first K/V pair issued: let this unit's Q tiles land
                     held = false;
                     for (int s2 = 0; s2 < 2 && ok; ++s2)
@@ -464,21 +484,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kTileBytes);
                     __syncwarp();
                     if constexpr (MODE == MODE_PAGED) {
-                        // lane = a * 8 + blk: one 16-token block of one 64-channel half
-                        if (lane < 8 * C::kAtoms) {
-                            const int a = lane >> 3, blk = lane & 7;
-                            const int lb = kt * 8 + blk;
-                            int phys = p.num_blocks;  // outside the map: zero fill
-                            if (lb * 16 < U.kv_len) {
-                                phys = __ldg(p.bt + (long)U.b * p.mbps + lb);
-                                if (phys < 0 || phys >= p.num_blocks) {
-                                    raise_error(p.ctx, ERR_BOUNDS_BIT);
-                                    phys = p.num_blocks;
-                                }
-                            }
-                            tma_load_4d(dst + a * C::kAtomBytes + blk * 2048, tm, &full[stage], a * 64, 0, U.hk,
-                                        phys);
-                        }
+                        if (lane < 8 * C::kAtoms)
+                            tma_load_4d(dst + (lane >> 3) * C::kAtomBytes + (lane & 7) * 2048, tm, &full[stage],
+                                        (lane >> 3) * 64, 0, U.hk, blk);
                     } else {
                         if (lane == 0) {
 #pragma unroll
