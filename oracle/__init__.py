@@ -76,7 +76,7 @@ def _load():
                                                  P, l, P, P, i]
         lib.ora_lse_merge.argtypes = [i, i, P, P, P, P]
         lib.ora_lse_merge.restype = None
-        lib.ora_mask_tile_classes.argtypes = [P, i, i, i, i, P]
+        lib.ora_mask_tile_classes.argtypes = [P, i, i, i, i, P, P]
         lib.ora_mask_tile_classes.restype = None
         _lib = lib
     return _lib
@@ -342,10 +342,14 @@ def lse_merge(O_parts, lse_parts):
     return O, float(lse[0])
 
 
-def mask_tile_classes(mask, bm: int = 128, bn: int = 128) -> np.ndarray:
-    """uint8 [ceil(Tq/bm), ceil(Tk/bn)]: 0 all -inf, 1 all zero, 2 mixed."""
+def mask_tile_classes(mask, bm: int = 128, bn: int = 128, intervals: bool = False):
+    """uint8 [ceil(Tq/bm), ceil(Tk/bn)]: 0 all -inf, 1 all zero, 3 every row's
+    zeros one contiguous run among -inf, 2 otherwise.  With intervals=True also
+    returns uint8 [ceil(Tq/bm), ceil(Tk/bn), bm, 2], each row's run [lo, hi) in
+    the class-3 tiles (zeros elsewhere)."""
     m = _f32(mask)
     Tq, Tk = m.shape
     out = np.zeros(((Tq + bm - 1) // bm, (Tk + bn - 1) // bn), dtype=np.uint8)
-    _load().ora_mask_tile_classes(_ptr(m), Tq, Tk, bm, bn, _ptr(out))
-    return out
+    iv = np.zeros(out.shape + (bm, 2), dtype=np.uint8)
+    _load().ora_mask_tile_classes(_ptr(m), Tq, Tk, bm, bn, _ptr(out), _ptr(iv))
+    return (out, iv) if intervals else out

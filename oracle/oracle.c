@@ -892,22 +892,57 @@ void ora_lse_merge(int nparts, int d, const double* O_parts, const double* lse_p
  * Class of each bm x bn tile of an additive mask [Tq, Tk] (edge tiles cover
  * only their in-range elements): 0 = every element -inf (the tile contributes
  * nothing), 1 = every element exactly 0 (the mask changes nothing there),
- * 2 = anything else.  cls: uint8 [ceil(Tq/bm), ceil(Tk/bn)].
+ * 3 = every element is 0 or -inf and, in every row, the columns holding 0 are
+ * one contiguous run (possibly empty) -- the tile restricts each row to an
+ * interval of keys and adds nothing else -- 2 = anything else.
+ * cls: uint8 [ceil(Tq/bm), ceil(Tk/bn)].  iv (may be NULL): uint8
+ * [ceil(Tq/bm), ceil(Tk/bn), bm, 2]; for a class-3 tile, row r of the tile
+ * gets (lo, hi), the run of zeros being columns [lo, hi) of the tile (lo = hi
+ * = 0 for a row of -inf only; rows past Tq get 0, 0); other tiles' entries are
+ * left as they are.  Needs bn <= 255.
  */
-void ora_mask_tile_classes(const float* M, int Tq, int Tk, int bm, int bn, uint8_t* cls)
+void ora_mask_tile_classes(const float* M, int Tq, int Tk, int bm, int bn, uint8_t* cls, uint8_t* iv)
 {
     int nti = (Tq + bm - 1) / bm, ntj = (Tk + bn - 1) / bn;
     for (int ti = 0; ti < nti; ++ti)
         for (int tj = 0; tj < ntj; ++tj) {
-            int all_neg_inf = 1, all_zero = 1;
-            for (int i = ti * bm; i < Tq && i < (ti + 1) * bm; ++i)
+            int all_neg_inf = 1, all_zero = 1, intervals = 1;
+            for (int i = ti * bm; i < Tq && i < (ti + 1) * bm; ++i) {
+                int first = -1, last = -1, zeros = 0;
                 for (int j = tj * bn; j < Tk && j < (tj + 1) * bn; ++j) {
                     float x = M[(long)i * Tk + j];
                     if (!(x == -INFINITY))
                         all_neg_inf = 0;
                     if (!(x == 0.0f))
                         all_zero = 0;
+                    if (x == 0.0f) {
+                        if (first < 0)
+                            first = j - tj * bn;
+                        last = j - tj * bn;
+                        ++zeros;
+                    } else if (!(x == -INFINITY)) {
+                        intervals = 0;
+                    }
                 }
-            cls[(long)ti * ntj + tj] = (uint8_t)(all_neg_inf ? 0 : (all_zero ? 1 : 2));
+                if (zeros > 0 && zeros != last - first + 1)
+                    intervals = 0;
+            }
+            uint8_t c = (uint8_t)(all_neg_inf ? 0 : (all_zero ? 1 : (intervals ? 3 : 2)));
+            cls[(long)ti * ntj + tj] = c;
+            if (c == 3 && iv) {
+                uint8_t* out = iv + ((long)ti * ntj + tj) * bm * 2;
+                for (int r = 0; r < bm; ++r) {
+                    int i = ti * bm + r, lo = 0, hi = 0;
+                    if (i < Tq)
+                        for (int j = tj * bn; j < Tk && j < (tj + 1) * bn; ++j)
+                            if (M[(long)i * Tk + j] == 0.0f) {
+                                if (hi == 0)
+                                    lo = j - tj * bn;
+                                hi = j - tj * bn + 1;
+                            }
+                    out[2 * r] = (uint8_t)lo;
+                    out[2 * r + 1] = (uint8_t)hi;
+                }
+            }
         }
 }

@@ -349,23 +349,51 @@ def test_cache_append_exact_with_canaries():
 
 # --------------------------------------------------------- mask classes ----
 def test_mask_tile_classes_recover_planted_map():
+    """Classes and row intervals planted tile by tile are what the oracle reads back."""
     rng = np.random.default_rng(4)
     Tq, Tk, bm, bn = 70, 90, 16, 32  # ragged edges on both axes
     nti, ntj = -(-Tq // bm), -(-Tk // bn)
-    planted = rng.integers(0, 3, size=(nti, ntj)).astype(np.uint8)
+    planted = rng.integers(0, 4, size=(nti, ntj)).astype(np.uint8)
+    planted[0, :3] = [0, 1, 3]  # every class at least once
+    planted[1, :2] = [2, 2]
+    want_iv = np.zeros((nti, ntj, bm, 2), np.uint8)
     M = np.zeros((Tq, Tk), np.float32)
     for ti in range(nti):
         for tj in range(ntj):
             blk = M[ti * bm:(ti + 1) * bm, tj * bn:(tj + 1) * bn]
+            rows, cols = blk.shape
             if planted[ti, tj] == 0:
                 blk[:] = -np.inf
             elif planted[ti, tj] == 2:
-                blk[:] = -np.inf  # one finite non-zero element makes the tile mixed
-                blk[rng.integers(0, blk.shape[0]), rng.integers(0, blk.shape[1])] = 0.5
-    got = oracle.mask_tile_classes(M, bm, bn)
+                blk[:] = -np.inf
+                if (ti + tj) % 2 and cols >= 3:  # a row with two separate runs of zeros
+                    r = rng.integers(0, rows)
+                    blk[r, 0] = 0.0
+                    blk[r, 2] = 0.0
+                else:  # one finite non-zero element
+                    blk[rng.integers(0, rows), rng.integers(0, cols)] = 0.5
+            elif planted[ti, tj] == 3:
+                blk[:] = -np.inf
+                for r in range(rows):
+                    lo = int(rng.integers(0, cols + 1))
+                    hi = int(rng.integers(lo, cols + 1))
+                    if r == 0:
+                        lo, hi = 0, max(1, cols - 1)  # not empty, not the whole row
+                    if r == 1 and rows > 2:
+                        lo, hi = 0, 0  # an empty row
+                    blk[r, lo:hi] = 0.0
+                    want_iv[ti, tj, r] = (lo, hi) if hi > lo else (0, 0)
+    got, iv = oracle.mask_tile_classes(M, bm, bn, intervals=True)
     assert np.array_equal(got, planted)
-    assert np.array_equal(oracle.mask_tile_classes(W.make_mask("causal_inf", 256, 256)),
-                          np.array([[2, 0], [1, 2]], np.uint8))
+    assert np.array_equal(oracle.mask_tile_classes(M, bm, bn), planted)
+    assert np.array_equal(iv[planted == 3], want_iv[planted == 3])
+    assert not iv[planted != 3].any()
+    # the causal mask: diagonal tiles restrict row r to keys [0, r + 1)
+    cls, iv = oracle.mask_tile_classes(W.make_mask("causal_inf", 256, 256), intervals=True)
+    assert np.array_equal(cls, np.array([[3, 0], [1, 3]], np.uint8))
+    for d in (0, 1):
+        assert np.array_equal(iv[d, d, :, 0], np.zeros(128, np.uint8))
+        assert np.array_equal(iv[d, d, :, 1], np.arange(1, 129, dtype=np.uint8))
 
 
 # ---------------------------------------------------- rotary + append -----
