@@ -137,8 +137,10 @@ fa_status fa_prefill_host(const void* q_host, const void* k_host, const void* v_
  *        Added to the causal mask when `causal` != 0.
  *   ws   device workspace of at least fa_prefill_masked_workspace_size(T)
  *        bytes; holds the per-tile mask classes (all -inf: tile skipped; all
- *        zero: mask not read; otherwise mask read and added) and the tile
- *        order.  Contents need not be initialised.
+ *        zero: mask not read; each row restricted to one run of keys: the run
+ *        applied as a column limit, mask not read; otherwise mask read and
+ *        added), the rows' runs and the tile order.  Contents need not be
+ *        initialised.
  */
 size_t fa_prefill_masked_workspace_size(int T);
 fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const float* mask,
@@ -151,15 +153,23 @@ fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const f
  * (the first pass of fa_prefill_masked, callable alone).
  * Passage: "FlashAttention-Style Kernels", attention equation with additive M
  * (a tile of M that is -inf everywhere contributes nothing; a tile that is 0
- * everywhere leaves the scores unchanged).
- *   mask fp32 [Tq, Tk] row-major, 16-byte aligned
- *   cls  uint8 [ceil(Tq/128), ceil(Tk/128)] row-major (written): 0 when every
- *        in-range element of the tile is -inf, 1 when every one is exactly 0
- *        (either sign), 2 otherwise; edge tiles cover only in-range elements
+ * everywhere leaves the scores unchanged; a tile of 0 and -inf only, whose
+ * zeros form one run in each row, only limits each row to an interval of keys).
+ *   mask      fp32 [Tq, Tk] row-major, 16-byte aligned
+ *   cls       uint8 [ceil(Tq/128), ceil(Tk/128)] row-major (written): 0 when
+ *             every in-range element of the tile is -inf, 1 when every one is
+ *             exactly 0 (either sign), 3 when every one is 0 or -inf and the
+ *             zeros of each row are one contiguous run (possibly empty), 2
+ *             otherwise; edge tiles cover only in-range elements
+ *   intervals NULL, or uint8 [ceil(Tq/128), ceil(Tk/128), 128, 2] (written for
+ *             class-3 tiles only): row r of the tile has its zeros at tile
+ *             columns [lo, hi) (lo = hi = 0 for a row without a zero and for
+ *             rows past Tq)
  * One read of M.  Empty masks are a no-op.  FA_ERR_UNSUPPORTED when Tq needs
  * more than 65535 tile rows.
  */
-fa_status fa_mask_tile_classes(const float* mask, int Tq, int Tk, uint8_t* cls, fa_stream_t stream);
+fa_status fa_mask_tile_classes(const float* mask, int Tq, int Tk, uint8_t* cls, uint8_t* intervals,
+                               fa_stream_t stream);
 
 /*
  * fa_stage_bf16 -- fp32 -> bf16 conversion, round to nearest even.  Used to

@@ -84,6 +84,7 @@ struct TcParams {
     // masked
     const float* mask;
     const uint8_t* cls;
+    const uint8_t* iv;  // per tile: 128 rows x (lo, hi), the run of keys a class-3 tile keeps
     const int32_t* qt_order;
     const int2* qt_range;  // per query tile: [first, last+1) of its KV tiles that are not all -inf;
                            // kRangeHoles set in .x when an all -inf tile lies inside that range
@@ -692,8 +693,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int vis_end = p.causal ? min(U.kv_len, row + U.pos_off + 1) : U.kv_len;
             float m = -INFINITY, l = 0.f;
             int it = 0;
+            // masked mode: this slot's class of the next tile and, for a class-3
+            // tile, this row's run of keys, read a tile ahead (a unit without
+            // holes visits every tile of its range)
+            const int nkt = (p.T + kTcRows - 1) / kTcRows;
+            auto row_run = [&](int kt) -> uchar2 {
+                return __ldg(reinterpret_cast<const uchar2*>(p.iv) +
+                             ((long)(sel(U.row0, s) / kTcRows) * nkt + kt) * kTcRows + r);
+            };
+            int cls_next = 0;
+            uchar2 run_next = make_uchar2(0, 0);
+            if constexpr (MODE == MODE_MASKED) {
+                cls_next = tile_class<MODE>(p, U, s, U.kt0);
+                if (cls_next == 3) run_next = row_run(U.kt0);
+            }
             for (int kt = U.kt0; kt < U.n_kt; ++kt) {
                 if (skip_tile<MODE>(p, U, kt)) continue;
+                int cls;
+                uchar2 run = make_uchar2(0, 0);
+                if constexpr (MODE == MODE_MASKED) {
+                    if (U.holes) {
+                        cls = tile_class<MODE>(p, U, s, kt);
+                        if (cls == 3) run = row_run(kt);
+                    } else {
+                        cls = cls_next;
+                        run = run_next;
+                        if (kt + 1 < U.n_kt) {
+                            cls_next = tile_class<MODE>(p, U, s, kt + 1);
+                            if (cls_next == 3) run_next = row_run(kt + 1);
+                        }
+                    }
+                } else {
+                    cls = tile_class<MODE>(p, U, s, kt);
+                }
                 if (!mbar_wait_warp(&sfull[s], sc & 1, lim_ns, abort_flag)) {
                     ok = false;
                     break;
@@ -702,7 +734,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after();
                 const int kv0 = kt * kTcRows;
                 const int lim = vis_end - kv0;  // visible columns of this tile: [0, lim)
-                const int cls = tile_class<MODE>(p, U, s, kt);
                 const float* mrow = (cls == 2 && valid) ? p.mask + (long)row * p.T + kv0 : nullptr;
                 // cls is the same for the whole warp (it depends on the slot and the
                 // tile only).  Without mask values (cls 0 or 1) the scores need only
@@ -711,9 +742,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // written back over S in pass 1 so that pass 2 reads them instead of
                 // re-reading the mask.
                 const bool general = cls == 2;
-                const int vlim = cls == 0 ? 0 : lim;  // visible columns of this row: [0, vlim)
+                // visible columns of this row: [vlo, vlim); a class-3 tile keeps
+                // the row's run of keys, applied like the causal limit (the
+                // limit path takes the general path's operations, so both give
+                // the same bits)
+                int vlo = 0, vlim = cls == 0 ? 0 : lim;
+                if constexpr (MODE == MODE_MASKED)
+                    if (cls == 3) {
+                        vlo = run.x;
+                        vlim = min(lim, (int)run.y);
+                    }
                 // every column of every row of the warp visible and no mask values
-                const bool plain = !general && __all_sync(0xffffffffu, vlim >= kTcRows);
+                const bool plain = !general && __all_sync(0xffffffffu, vlo == 0 && vlim >= kTcRows);
                 // pass 1: row max.  Without mask values the whole 128-column score row
                 // is loaded with one TMEM wait; the general case takes 64 columns per
                 // wait.  8 independent partial maxima / sums keep the reductions off a
@@ -735,8 +775,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     } else {
 #pragma unroll
                         for (int j = 0; j < kTcRows; j += 2)
-                            mxp[(j >> 1) & 7] = fmax3f(mxp[(j >> 1) & 7], j < vlim ? __uint_as_float(raw[j]) : -INFINITY,
-                                                       j + 1 < vlim ? __uint_as_float(raw[j + 1]) : -INFINITY);
+                            mxp[(j >> 1) & 7] =
+                                fmax3f(mxp[(j >> 1) & 7], j >= vlo && j < vlim ? __uint_as_float(raw[j]) : -INFINITY,
+                                       j + 1 >= vlo && j + 1 < vlim ? __uint_as_float(raw[j + 1]) : -INFINITY);
                     }
                 } else {
                     const bool vec_mask = mrow && ((p.T & 3) == 0);
@@ -828,8 +869,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const float2 x = __ffma2_rn(make_float2(fmaf(__uint_as_float(raw[2 * j]), p.scale_log2, 0.f),
                                                                     fmaf(__uint_as_float(raw[2 * j + 1]), p.scale_log2, 0.f)),
                                                         make_float2(1.f, 1.f), neg_m);
-                            const float2 pp = make_float2(c0 + 2 * j < vlim ? fast_exp2(x.x) : 0.f,
-                                                          c0 + 2 * j + 1 < vlim ? fast_exp2(x.y) : 0.f);
+                            const int cj = c0 + 2 * j;
+                            const float2 pp = make_float2(cj >= vlo && cj < vlim ? fast_exp2(x.x) : 0.f,
+                                                          cj + 1 >= vlo && cj + 1 < vlim ? fast_exp2(x.y) : 0.f);
                             rsp[j & 3] = __fadd2_rn(rsp[j & 3], pp);
                             pk[j] = pack_bf16x2(pp.x, pp.y);
                         }
@@ -920,7 +962,7 @@ __global__ void __launch_bounds__(256) mask_order_kernel(const uint8_t* __restri
     }
 }
 
-fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, cudaStream_t s);
+fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, uint8_t* iv, cudaStream_t s);
 
 // ------------------------------------------------------------ launchers ---
 template <int D, int MODE>
@@ -1176,7 +1218,7 @@ fa_status fa_prefill_rows(const void* q, const void* k, const void* v, void* out
 size_t fa_prefill_masked_workspace_size(int T) {
     if (T <= 0) return 0;
     const size_t nt = (size_t)(T + kTcRows - 1) / kTcRows;
-    return align256(nt * nt) + align256(sizeof(int32_t) * nt) + align256(sizeof(int2) * nt);
+    return align256(nt * nt) + align256(sizeof(int32_t) * nt) + align256(sizeof(int2) * nt) + align256(nt * nt * 256);
 }
 
 fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const float* mask, void* out, int B, int T,
@@ -1199,7 +1241,9 @@ fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const f
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + align256((size_t)nt * nt));
     int2* range = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + align256((size_t)nt * nt) +
                                           align256(sizeof(int32_t) * nt));
-    if ((st = launch_mask_classify(mask, T, T, cls, s)) != FA_OK) return st;
+    uint8_t* iv = static_cast<uint8_t*>(ws) + align256((size_t)nt * nt) + align256(sizeof(int32_t) * nt) +
+                  align256(sizeof(int2) * nt);
+    if ((st = launch_mask_classify(mask, T, T, cls, iv, s)) != FA_OK) return st;
     if ((size_t)nt * sizeof(int) > 200 * 1024) return FA_ERR_UNSUPPORTED;
     if (nt * sizeof(int) > 48 * 1024 &&
         (st = raise_dynamic_smem(reinterpret_cast<const void*>(mask_order_kernel), nt * (int)sizeof(int))) != FA_OK)
@@ -1209,6 +1253,7 @@ fa_status fa_prefill_masked(const void* q, const void* k, const void* v, const f
     TcParams p = base_params(B, T, Hq, Hkv, causal, scale, out, lse, ctx);
     p.mask = mask;
     p.cls = cls;
+    p.iv = iv;
     p.qt_order = order;
     p.qt_range = range;
     p.num_units = dense_units(p);

@@ -269,40 +269,87 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint16_t* __restri
 }
 
 // ------------------------------------------------------- mask classes -----
-// One CTA per 128x128 tile of the mask: class 0 when every in-range element
-// is -inf, 1 when every element is exactly 0, 2 otherwise.  Rows are read
-// with coalesced 16-byte loads when the row length allows it.
+// One CTA per 128x128 tile of the mask (edge tiles: their in-range elements):
+// class 0 when every element is -inf, 1 when every element is exactly 0, 3
+// when every element is 0 or -inf and the zeros of each row are one
+// contiguous run (possibly empty) -- the tile only restricts each query row to
+// an interval of keys -- and 2 otherwise.  For a class-3 tile, iv (when not
+// null) gets each of the 128 rows' run [lo, hi) as two bytes, at
+// iv[((ti * ntj + tj) * 128 + r) * 2] (rows past Tq, and rows without a zero,
+// get 0, 0).  Every tile is read once with coalesced 16-byte loads when the
+// row length allows; only the tiles of 0 and -inf that are neither all 0 nor
+// all -inf are read a second time, row by row, for the runs.
 __global__ void __launch_bounds__(256) mask_classify_kernel(const float* __restrict__ M, int Tq, int Tk,
-                                                            uint8_t* __restrict__ cls) {
+                                                            uint8_t* __restrict__ cls, uint8_t* __restrict__ iv) {
+    __shared__ uint8_t run[128][2];
     const int tj = blockIdx.x, ti = blockIdx.y;
     const int i0 = ti * 128, j0 = tj * 128;
     const int rows = min(128, Tq - i0), cols = min(128, Tk - j0);
-    bool all_ninf = true, all_zero = true;
+    const int lane = threadIdx.x & 31, rgrp = threadIdx.x >> 5;
     const bool vec = (Tk % 4 == 0) && (cols == 128);
+    // pass 1: is every element -inf, is every element 0, is any element
+    // neither (one read of the tile)
+    bool all_ninf = true, all_zero = true, only_0_inf = true;
+    auto take = [&](float x) {
+        all_ninf &= (x == -INFINITY);
+        all_zero &= (x == 0.f);
+        only_0_inf &= (x == 0.f) | (x == -INFINITY);
+    };
     if (vec) {
         // 32 threads cover one 512-byte row; 8 rows per pass
-        const int lane = threadIdx.x & 31, rgrp = threadIdx.x >> 5;
         for (int r = rgrp; r < rows; r += 8) {
-            float4 x = __ldg(reinterpret_cast<const float4*>(M + (long)(i0 + r) * Tk + j0) + lane);
-            all_ninf &= (x.x == -INFINITY) & (x.y == -INFINITY) & (x.z == -INFINITY) & (x.w == -INFINITY);
-            all_zero &= (x.x == 0.f) & (x.y == 0.f) & (x.z == 0.f) & (x.w == 0.f);
+            const float4 x = __ldg(reinterpret_cast<const float4*>(M + (long)(i0 + r) * Tk + j0) + lane);
+            take(x.x);
+            take(x.y);
+            take(x.z);
+            take(x.w);
         }
     } else {
-        for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
-            const float x = __ldg(M + (long)(i0 + e / cols) * Tk + j0 + e % cols);
-            all_ninf &= (x == -INFINITY);
-            all_zero &= (x == 0.f);
-        }
+        for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) take(__ldg(M + (long)(i0 + e / cols) * Tk + j0 + e % cols));
     }
     const int n_inf = __syncthreads_and(all_ninf);
     const int n_zero = __syncthreads_and(all_zero);
-    if (threadIdx.x == 0) cls[(long)ti * gridDim.x + tj] = (uint8_t)(n_inf ? 0 : (n_zero ? 1 : 2));
+    const int n_01 = __syncthreads_and(only_0_inf);
+    uint8_t c = (uint8_t)(n_inf ? 0 : (n_zero ? 1 : 2));
+    if (c == 2 && n_01) {
+        // pass 2 (tiles of 0 and -inf only, both present): one warp per row
+        // re-reads the row (from L2) and finds its first and last zero and the
+        // number of zeros; the row keeps one run of keys when they agree
+        bool runs = true;
+        for (int r = rgrp; r < 128; r += 8) {
+            int lo = 0, hi = 0;
+            if (r < rows) {
+                int zeros = 0, first = 128, last = -1;
+                for (int j = lane; j < cols; j += 32)
+                    if (__ldg(M + (long)(i0 + r) * Tk + j0 + j) == 0.f) {
+                        first = min(first, j);
+                        last = j;
+                        ++zeros;
+                    }
+                zeros = __reduce_add_sync(0xffffffffu, zeros);
+                if (zeros > 0) {
+                    lo = __reduce_min_sync(0xffffffffu, first);
+                    hi = __reduce_max_sync(0xffffffffu, last) + 1;
+                    runs &= zeros == hi - lo;
+                }
+            }
+            if (lane == 0) {
+                run[r][0] = (uint8_t)lo;
+                run[r][1] = (uint8_t)hi;
+            }
+        }
+        if (__syncthreads_and(runs)) c = 3;
+    }
+    const long tile = (long)ti * gridDim.x + tj;
+    if (threadIdx.x == 0) cls[tile] = c;
+    if (c == 3 && iv)
+        for (int e = threadIdx.x; e < 256; e += blockDim.x) iv[tile * 256 + e] = run[e >> 1][e & 1];
 }
 
 // Launched from the masked prefill entry point.
-fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, cudaStream_t s) {
+fa_status launch_mask_classify(const float* M, int Tq, int Tk, uint8_t* cls, uint8_t* iv, cudaStream_t s) {
     dim3 grid((Tk + 127) / 128, (Tq + 127) / 128);
-    mask_classify_kernel<<<grid, 256, 0, s>>>(M, Tq, Tk, cls);
+    mask_classify_kernel<<<grid, 256, 0, s>>>(M, Tq, Tk, cls, iv);
     return cuda_status(cudaGetLastError());
 }
 
@@ -347,7 +394,8 @@ fa_status fa_cache_append(const void* k, const void* v, void* k_cache, void* v_c
     return st;
 }
 
-fa_status fa_mask_tile_classes(const float* mask, int Tq, int Tk, uint8_t* cls, fa_stream_t stream) {
+fa_status fa_mask_tile_classes(const float* mask, int Tq, int Tk, uint8_t* cls, uint8_t* intervals,
+                               fa_stream_t stream) {
     set_launch_count(0);
     if (Tq < 0 || Tk < 0) return FA_ERR_INVALID_ARG;
     if (Tq == 0 || Tk == 0) return FA_OK;
@@ -355,7 +403,7 @@ fa_status fa_mask_tile_classes(const float* mask, int Tq, int Tk, uint8_t* cls, 
     if ((Tq + 127) / 128 > 65535) return FA_ERR_UNSUPPORTED;  // grid y limit
     fa_status st = check_device();
     if (st != FA_OK) return st;
-    st = launch_mask_classify(mask, Tq, Tk, cls, reinterpret_cast<cudaStream_t>(stream));
+    st = launch_mask_classify(mask, Tq, Tk, cls, intervals, reinterpret_cast<cudaStream_t>(stream));
     if (st == FA_OK) set_launch_count(1);
     return st;
 }

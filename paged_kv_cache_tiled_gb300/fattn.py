@@ -56,7 +56,7 @@ def _load() -> ctypes.CDLL:
         "fa_prefill_masked_workspace_size": (Z, [I]),
         "fa_prefill_masked": (I, [P, P, P, P, P, I, I, I, I, I, I, F, P, P, Z, P]),
         "fa_stage_bf16": (I, [P, P, Z, P]),
-        "fa_mask_tile_classes": (I, [P, I, I, P, P]),
+        "fa_mask_tile_classes": (I, [P, I, I, P, P, P]),
         "fa_cache_append": (I, [P, P, P, P, P, I, I, I, I, I, P]),
         "fa_paged_attn_workspace_size": (Z, [I, I, I, I, I, I]),
         "fa_paged_attn": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, Z, P]),
@@ -219,8 +219,10 @@ def fa_prefill_masked(q, k, v, mask, causal: bool = False, scale: float | None =
     return out
 
 
-def fa_mask_tile_classes(mask, out=None, stream=None):
-    """uint8 [ceil(Tq/128), ceil(Tk/128)] classes of an fp32 mask [Tq, Tk]: 0 all -inf, 1 all zero, 2 mixed."""
+def fa_mask_tile_classes(mask, out=None, intervals=None, stream=None):
+    """uint8 [ceil(Tq/128), ceil(Tk/128)] classes of an fp32 mask [Tq, Tk]: 0 all -inf, 1 all zero,
+    3 zeros forming one run per row among -inf, 2 otherwise.  `intervals` (optional, uint8
+    [ceil(Tq/128), ceil(Tk/128), 128, 2]) receives each row's run [lo, hi) in class-3 tiles."""
     _need(mask, "mask", torch.float32, 2)
     Tq, Tk = mask.shape
     shape = ((Tq + 127) // 128, (Tk + 127) // 128)
@@ -229,7 +231,12 @@ def fa_mask_tile_classes(mask, out=None, stream=None):
     _need(out, "out", torch.uint8, 2)
     if tuple(out.shape) != shape:
         raise ValueError(f"out must have shape {shape}")
-    _check(_lib.fa_mask_tile_classes(_ptr(mask), Tq, Tk, _ptr(out), _stream(stream)), "fa_mask_tile_classes")
+    if intervals is not None:
+        _need(intervals, "intervals", torch.uint8, 4)
+        if tuple(intervals.shape) != shape + (128, 2):
+            raise ValueError(f"intervals must have shape {shape + (128, 2)}")
+    _check(_lib.fa_mask_tile_classes(_ptr(mask), Tq, Tk, _ptr(out), _ptr(intervals) if intervals is not None else None,
+                                     _stream(stream)), "fa_mask_tile_classes")
     return out
 
 

@@ -113,13 +113,22 @@ def test_mask_tile_classes_match_oracle(F, T, kind):
 @pytest.mark.parametrize("Tq,Tk", [(300, 300), (128, 640), (257, 129), (1, 3)])
 @pytest.mark.parametrize("kind", ["random", "band", "causal_inf"])
 def test_mask_tile_classes_entry_point(F, Tq, Tk, kind):
-    """The standalone class pass equals the oracle on ragged and non-square masks."""
+    """The standalone class pass equals the oracle on ragged and non-square masks, classes
+    and the class-3 tiles' row runs."""
     mask = W.make_mask(kind, Tq, Tk, 11)
     if kind == "random":  # plant all-zero and all--inf tiles among the mixed ones
         mask[:128, :128] = 0.0
         if Tk > 128:
             mask[:, 128:256] = float("-inf")
-    got = F.fa_mask_tile_classes(mask.cuda())
+    shape = ((Tq + 127) // 128, (Tk + 127) // 128)
+    iv = torch.full(shape + (128, 2), 7, dtype=torch.uint8, device="cuda")  # 7: left untouched
+    got = F.fa_mask_tile_classes(mask.cuda(), intervals=iv).cpu().numpy()
     assert F.fa_get_error() == F.FA_OK
-    assert np.array_equal(got.cpu().numpy(), oracle.mask_tile_classes(mask))
+    want, want_iv = oracle.mask_tile_classes(mask, intervals=True)
+    assert np.array_equal(got, want)
+    iv = iv.cpu().numpy()
+    assert np.array_equal(iv[want == 3], want_iv[want == 3])  # each row's run of kept keys
+    assert (iv[want != 3] == 7).all()
+    if kind == "causal_inf" and Tq > 1:  # the diagonal tiles keep a run of keys per row
+        assert (want == 3).any()
 
