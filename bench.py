@@ -49,8 +49,8 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# the sources the profiled kernels (attn_tc_kernel, paged_decode_kernel) are built from
-PROFILED_SOURCES = ("attn_tc.cu", "paged.cu", "common.cuh", "host_common.cuh")
+# the sources the profiled kernels (attn_tc_kernel, paged_decode_kernel, mask_classify_kernel) are built from
+PROFILED_SOURCES = ("attn_tc.cu", "paged.cu", "cache_ops.cu", "common.cuh", "host_common.cuh")
 
 
 def kernel_source_hash():
