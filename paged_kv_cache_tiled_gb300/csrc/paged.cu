@@ -783,6 +783,29 @@ __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restr
     }
 }
 
+// A library-owned side stream per device: the chunked-prefill metadata pass (one
+// CTA) runs there beside the split-KV decode kernel and its merge, which do
+// not depend on it; two events fork it from and join it back to the caller's
+// stream (both capturable, so the call may be recorded into a CUDA graph).
+constexpr int kMaxSideDevices = 64;
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxSideDevices];
+
+static fa_status side_stream(SideStream** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return FA_ERR_CUDA;
+    SideStream& ss = g_side[dev];
+    if (!ss.s && cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return FA_ERR_CUDA;
+    if (!ss.fork && cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
+    if (!ss.join && cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
+    *out = &ss;
+    return FA_OK;
+}
+
 template <int D, bool KV8 = false>
 static fa_status launch_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* bt,
                                const int32_t* ctx_lens, const int32_t* q_lens, void* out, const PagedWs& w,
@@ -876,18 +899,13 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     const int g = Hq / Hkv;
     int launches = 0;
-    if (g <= kDecodeRows) {
-        const int merge_rows = (int)std::min<long>(kDecodeRows, (long)g * max_q_len);
-        const int qpf = is_decode_row(max_q_len, g) ? total_q : 0;  // every query row is a decode row
-        st = d == 128 ? launch_decode<128>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
-                                           max_blocks_per_seq, num_blocks, Hq, Hkv, qpf, causal, scale, merge_rows, s,
-                                           ctx, &launches)
-                      : launch_decode<64>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
-                                          max_blocks_per_seq, num_blocks, Hq, Hkv, qpf, causal, scale, merge_rows, s,
-                                          ctx, &launches);
-        if (st != FA_OK) return st;
-    }
-    if (!is_decode_row(max_q_len, g)) {
+    const bool decode_path = g <= kDecodeRows;  // some sequences may be decode rows
+    const bool tc_path = !is_decode_row(max_q_len, g);
+    // the tensor-core path's work list: on the side stream when the decode
+    // kernel also runs (they are independent), else in line
+    SideStream* ss = nullptr;
+    std::unique_lock<std::mutex> side_lock;
+    if (tc_path) {
         const int entry_tokens = paged_tc_entry_tokens(g);
         int32_t* q_start = reinterpret_cast<int32_t*>(wsb + w.q_start);
         int32_t* count = reinterpret_cast<int32_t*>(wsb + w.work_count);
@@ -898,10 +916,43 @@ fa_status fa_paged_attn(const void* q, const void* k_cache, const void* v_cache,
         if (hist_bytes > 48 * 1024 &&
             (st = raise_dynamic_smem(reinterpret_cast<const void*>(paged_meta_kernel), (int)hist_bytes)) != FA_OK)
             return st;
-        paged_meta_kernel<<<1, 1024, hist_bytes, s>>>(ctx_lens, q_lens, num_seqs, max_blocks_per_seq, g, causal,
-                                                      entry_tokens, q_start, count, list, w.max_entries, ctx);
-        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+        cudaStream_t ms = s;
+        if (decode_path) {
+            if ((st = side_stream(&ss)) != FA_OK) return st;
+            side_lock = std::unique_lock<std::mutex>(ss->mu);
+            if (cudaEventRecord(ss->fork, s) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+                return FA_ERR_CUDA;
+            ms = ss->s;
+        }
+        paged_meta_kernel<<<1, 1024, hist_bytes, ms>>>(ctx_lens, q_lens, num_seqs, max_blocks_per_seq, g, causal,
+                                                       entry_tokens, q_start, count, list, w.max_entries, ctx);
+        const bool launched = cudaGetLastError() == cudaSuccess;
+        if (ss && (cudaEventRecord(ss->join, ss->s) != cudaSuccess || !launched)) {
+            (void)cudaStreamWaitEvent(s, ss->join, 0);  // leave the side stream joined
+            return FA_ERR_CUDA;
+        }
+        if (!launched) return FA_ERR_CUDA;
         ++launches;
+    }
+    if (decode_path) {
+        const int merge_rows = (int)std::min<long>(kDecodeRows, (long)g * max_q_len);
+        const int qpf = is_decode_row(max_q_len, g) ? total_q : 0;  // every query row is a decode row
+        st = d == 128 ? launch_decode<128>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
+                                           max_blocks_per_seq, num_blocks, Hq, Hkv, qpf, causal, scale, merge_rows, s,
+                                           ctx, &launches)
+                      : launch_decode<64>(q, k_cache, v_cache, block_table, ctx_lens, q_lens, out, w, wsb, num_seqs,
+                                          max_blocks_per_seq, num_blocks, Hq, Hkv, qpf, causal, scale, merge_rows, s,
+                                          ctx, &launches);
+        if (st != FA_OK) {
+            if (ss) (void)cudaStreamWaitEvent(s, ss->join, 0);  // keep the side stream joined
+            return st;
+        }
+    }
+    if (tc_path) {
+        if (ss && cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess) return FA_ERR_CUDA;
+        int32_t* q_start = reinterpret_cast<int32_t*>(wsb + w.q_start);
+        int32_t* count = reinterpret_cast<int32_t*>(wsb + w.work_count);
+        int32_t* list = reinterpret_cast<int32_t*>(wsb + w.work_list);
         st = launch_paged_prefill(q, k_cache, v_cache, block_table, ctx_lens, q_lens, q_start, list, count, out,
                                   num_seqs, max_blocks_per_seq, num_blocks, Hq, Hkv, d, causal, scale, total_q, s,
                                   ctx);
