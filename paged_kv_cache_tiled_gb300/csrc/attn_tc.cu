@@ -373,7 +373,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&empty[i], 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&qfull[s], 1);
             mbar_init(&qempty[s], 1);
             mbar_init(&sfull[s], 1);
             mbar_init(&pfull[2 * s], kTcRows);
@@ -385,10 +384,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *abort_flag = 0;
         mbar_fence_init();
     }
+    // The producer's first lane owns the Q barriers' set-up and requests the
+    // first unit's Q tiles before the set-up barrier, so that their copies
+    // overlap the TMEM allocation and the barrier itself.
     if (warp == kProducerWarp && lane == 0) {
+        mbar_init(&qfull[0], 1);
+        mbar_init(&qfull[1], 1);
+        mbar_fence_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        int n0;
+        if constexpr (MODE == MODE_PAGED)
+            n0 = __ldg(p.work_count) * paged_units_per_entry(p);
+        else
+            n0 = p.num_units;
+        const int u0 = cta_unit(sched, 0, gridDim.x, n0);
+        if (u0 >= 0) {
+            const Unit U0 = decode_unit<MODE>(p, u0);
+            if (unit_active<MODE>(p, U0))
+                for (int s = 0; s < 2; ++s) {
+                    mbar_arrive_expect_tx(&qfull[s], C::kTileBytes);
+#pragma unroll
+                    for (int a = 0; a < C::kAtoms; ++a) {
+                        if constexpr (MODE == MODE_PAGED)
+                            tma_load_4d(qbuf + s * C::kTileBytes + a * C::kAtomBytes, &tm_q, &qfull[s], a * 64,
+                                        sel(U0.head, s), sel(U0.qtok, s), 0);
+                        else
+                            tma_load_4d(qbuf + s * C::kTileBytes + a * C::kAtomBytes, &tm_q, &qfull[s], a * 64,
+                                        sel(U0.head, s), sel(U0.qtok, s), U0.b);
+                    }
+                }
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
@@ -426,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             if (!unit_active<MODE>(p, U)) continue;
-            for (int s = 0; s < 2 && ok; ++s) {
+            for (int s = 0; s < 2 && ok && i > 0; ++s) {  // unit 0's Q tiles were requested at the start
                 if (!mbar_wait_warp(&qempty[s], (qcnt & 1) ^ 1, lim_ns, abort_flag)) {
                     ok = false;
                     break;
@@ -506,9 +533,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // let every copy already issued land before the CTA can exit
             for (int f = max(0, fill - S); f < fill; ++f)
                 (void)mbar_wait_warp(&full[f % S], (f / S) & 1, 1000000000ull, nullptr);
-            if (qcnt > 0)
+            // unit 0's Q tiles may be in flight even if the loop never ran
+            bool q0 = false;
+            if (qcnt == 0) {
+                const int u0 = cta_unit(sched, 0, G, num_units);
+                q0 = u0 >= 0 && unit_active<MODE>(p, decode_unit<MODE>(p, u0));
+            }
+            if (qcnt > 0 || q0)
                 for (int s = 0; s < 2; ++s)
-                    (void)mbar_wait_warp(&qfull[s], (qcnt - 1) & 1, 1000000000ull, nullptr);
+                    (void)mbar_wait_warp(&qfull[s], qcnt > 0 ? (qcnt - 1) & 1 : 0, 1000000000ull, nullptr);
         }
     } else if (warp == kMmaWarp) {
         // ===================================================== MMA issuer ===
