@@ -341,6 +341,50 @@ __device__ __noinline__ void scale_tmem_row(uint32_t taddr, float alpha) {
     tmem_wait_st();
 }
 
+// Pass 1 of the softmax for a tile with additive mask values (class 2): reads
+// this thread's 128-column score row from TMEM at taddr, writes back the
+// logits s * scale_log2 + M * log2(e) (-inf at columns >= lim), and returns
+// their maximum.  mrow: the row's mask values for this tile (null: none);
+// vec_mask: they may be read 16 bytes at a time.  Out of line: general tiles
+// are rare, and the inlined code slowed every other tile of the loop (and the
+// dense kernel, which compiles the same loop).
+__device__ __noinline__ float masked_logits_row(uint32_t taddr, const float* mrow, int lim, float scale_log2,
+                                                bool vec_mask) {
+    float mxp[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint32_t raw[64];
+        tmem_ld32(taddr + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+        tmem_ld32(taddr + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+        tmem_wait_ld();
+#pragma unroll
+        for (int j4 = 0; j4 < 16; ++j4) {
+            float mv[4] = {0.f, 0.f, 0.f, 0.f};
+            const int j0 = h * 64 + 4 * j4;
+            if (vec_mask && j0 + 3 < lim) {
+                const float4 t = __ldg(reinterpret_cast<const float4*>(mrow + j0));
+                mv[0] = t.x; mv[1] = t.y; mv[2] = t.z; mv[3] = t.w;
+            } else if (mrow) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mv[e] = (j0 + e < lim) ? __ldg(mrow + j0 + e) : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = j0 + e;
+                const float x = j >= lim ? -INFINITY : fmaf(__uint_as_float(raw[4 * j4 + e]), scale_log2, mv[e] * kLog2e);
+                raw[4 * j4 + e] = __float_as_uint(x);
+                mxp[(4 * j4 + e) & 7] = fmaxf(mxp[(4 * j4 + e) & 7], x);
+            }
+        }
+        tmem_st32(taddr + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
+        tmem_st32(taddr + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+    }
+    tmem_wait_st();
+    return fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])), fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+}
+
 // ------------------------------------------------------------------ kernel --
 template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -813,38 +857,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                        j + 1 >= vlo && j + 1 < vlim ? __uint_as_float(raw[j + 1]) : -INFINITY);
                     }
                 } else {
-                    const bool vec_mask = mrow && ((p.T & 3) == 0);
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t raw[64];
-                        tmem_ld32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
-                        tmem_ld32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j4 = 0; j4 < 16; ++j4) {
-                            float mv[4] = {0.f, 0.f, 0.f, 0.f};
-                            const int j0 = h * 64 + 4 * j4;
-                            if (vec_mask && j0 + 3 < lim) {
-                                const float4 t = __ldg(reinterpret_cast<const float4*>(mrow + j0));
-                                mv[0] = t.x; mv[1] = t.y; mv[2] = t.z; mv[3] = t.w;
-                            } else if (mrow) {
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) mv[e] = (j0 + e < lim) ? __ldg(mrow + j0 + e) : 0.f;
-                            }
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int j = j0 + e;
-                                const float x = j >= lim
-                                                    ? -INFINITY
-                                                    : fmaf(__uint_as_float(raw[4 * j4 + e]), p.scale_log2, mv[e] * kLog2e);
-                                raw[4 * j4 + e] = __float_as_uint(x);
-                                mxp[(4 * j4 + e) & 7] = fmaxf(mxp[(4 * j4 + e) & 7], x);
-                            }
-                        }
-                        tmem_st32(trow + s_col + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
-                        tmem_st32(trow + s_col + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
-                    }
-                    tmem_wait_st();
+                    mxp[0] = masked_logits_row(trow + s_col, mrow, lim, p.scale_log2, mrow && ((p.T & 3) == 0));
                 }
                 float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                  fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
