@@ -329,6 +329,7 @@ __device__ __noinline__ void zero_tile_rows(uint8_t* base, int z0, int z1) {
 // 3 % on short prefills.
 template <int D>
 __device__ __noinline__ void scale_tmem_row(uint32_t taddr, float alpha) {
+    __syncwarp();  // warp-collective TMEM accesses follow
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -356,6 +357,7 @@ __device__ __noinline__ float masked_logits_row(uint32_t taddr, const float* mro
 #pragma unroll 1
     for (int h = 0; h < 2; ++h) {
         uint32_t raw[64];
+        __syncwarp();  // the TMEM accesses are warp-collective; the mask loads below may diverge
         tmem_ld32(taddr + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
         tmem_ld32(taddr + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
         tmem_wait_ld();
@@ -378,6 +380,7 @@ __device__ __noinline__ float masked_logits_row(uint32_t taddr, const float* mro
                 mxp[(4 * j4 + e) & 7] = fmaxf(mxp[(4 * j4 + e) & 7], x);
             }
         }
+        __syncwarp();
         tmem_st32(taddr + h * 64, *reinterpret_cast<uint32_t(*)[32]>(raw));
         tmem_st32(taddr + h * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
     }

@@ -64,6 +64,44 @@ def test_dense_parity(F, shape):
     assert_parity(lse, ref_lse, f"lse {shape}")
 
 
+def growing_scores_case(B, T, Hq, Hkv, d, seed=5):
+    """q = u for every row and k_j = (j / 8) u with |u|^2 = sqrt(d): the score of key
+    j is j / 8 for every query, so each 128-key tile raises a row's running maximum
+    by 16 (23 in log2 units), past the rescale threshold on every tile."""
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal(d)
+    u *= np.sqrt(np.sqrt(d)) / np.linalg.norm(u)
+    j = np.arange(T, dtype=np.float64) / 8.0
+    q = np.broadcast_to(u, (B, T, Hq, d)).copy()
+    k = np.broadcast_to((j[:, None] * u)[None, :, None, :], (B, T, Hkv, d)).copy()
+    v = rng.standard_normal((B, T, Hkv, d))
+    to = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    return to(q), to(k), to(v)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_running_max_rescale_on_every_tile(F, causal):
+    """Scores that grow along the keys make every KV tile rescale the output
+    accumulator in place (the softmax's rare path); the result still matches the
+    oracle, densely and through the paged cache."""
+    B, T, Hq, Hkv, d = 1, 1024, 4, 1, 128
+    q, k, v = growing_scores_case(B, T, Hq, Hkv, d)
+    scale = 1.0 / np.sqrt(d)
+    out = F.fa_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    assert F.fa_get_error() == F.FA_OK
+    ref, _ = oracle.attention(q, k, v, causal, scale)
+    assert_parity(out, ref, f"growing scores, dense, causal={causal}")
+    # the same sequence through the paged cache (one sequence, table 0 1 2 ...)
+    nb = T // 16
+    kc = k[0].reshape(nb, 16, Hkv, d).permute(0, 2, 1, 3).contiguous().cuda()
+    vc = v[0].reshape(nb, 16, Hkv, d).permute(0, 2, 1, 3).contiguous().cuda()
+    bt = torch.arange(nb, dtype=torch.int32).reshape(1, nb).cuda()
+    lens = torch.tensor([T], dtype=torch.int32).cuda()
+    out_p = F.fa_paged_attn(q[0].contiguous().cuda(), kc, vc, bt, lens, lens, causal=causal, scale=scale, max_q_len=T)
+    assert F.fa_get_error() == F.FA_OK
+    assert_parity(out_p, ref[0], f"growing scores, paged, causal={causal}")
+
+
 def test_config2_full_size(F):
     """Config 2 at full size (B=4, T=2048, Hq=12, Hkv=2, d=128), every element."""
     case = W.config2()
