@@ -989,18 +989,25 @@ __global__ void __launch_bounds__(256) mask_order_kernel(const uint8_t* __restri
                                                          int causal, int32_t* __restrict__ order,
                                                          int2* __restrict__ range) {
     extern __shared__ int cost[];
-    for (int q = threadIdx.x; q < nqt; q += blockDim.x) {
+    // one warp per query tile, 32 of its classes per (coalesced) step
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int q = threadIdx.x >> 5; q < nqt; q += nw) {
         int c = 0, lo = nkt, hi = 0;
         const int kend = causal ? min(nkt, q + 1) : nkt;
-        for (int k = 0; k < kend; ++k)
-            if (cls[(long)q * nkt + k] != 0) {
-                ++c;
-                lo = min(lo, k);
-                hi = k + 1;
+        for (int k0 = 0; k0 < kend; k0 += 32) {
+            const int k = k0 + lane;
+            const unsigned vis = __ballot_sync(0xffffffffu, k < kend && cls[(long)q * nkt + k] != 0);
+            if (vis) {
+                c += __popc(vis);
+                if (lo == nkt) lo = k0 + __ffs(vis) - 1;
+                hi = k0 + 32 - __clz(vis);
             }
-        cost[q] = c;
-        // flag: an all -inf tile inside [lo, hi) (the scan must check classes)
-        range[q] = make_int2(lo | (c > 0 && c < hi - lo ? kRangeHoles : 0), hi);
+        }
+        if (lane == 0) {
+            cost[q] = c;
+            // flag: an all -inf tile inside [lo, hi) (the scan must check classes)
+            range[q] = make_int2(lo | (c > 0 && c < hi - lo ? kRangeHoles : 0), hi);
+        }
     }
     __syncthreads();
     for (int q = threadIdx.x; q < nqt; q += blockDim.x) {
