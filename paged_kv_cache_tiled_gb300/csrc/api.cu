@@ -111,26 +111,42 @@ fa_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t
                           CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The driver's tensor-map encoder, looked up once (null if unavailable).
+static EncodeTiledFn encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess && fn)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
 fa_status encode_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
                          const uint32_t box[4], CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle) {
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_encode) {
-            void* fn = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                    cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || !fn)
-                return FA_ERR_CUDA;
-            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-        }
-    }
+    if (!encoder()) return FA_ERR_CUDA;
     cuuint64_t gdim[4] = {dims[0], dims[1], dims[2], dims[3]};
     cuuint64_t gstr[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
     cuuint32_t bdim[4] = {box[0], box[1], box[2], box[3]};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(map, dtype, 4, const_cast<void*>(base), gdim, gstr, bdim, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
+fa_status encode_tmap_bf16_5d(CUtensorMap* map, const void* base, const uint64_t dims[5], const uint64_t strides_bytes[4],
+                              const uint32_t box[5]) {
+    if (!encoder()) return FA_ERR_CUDA;
+    cuuint64_t gdim[5] = {dims[0], dims[1], dims[2], dims[3], dims[4]};
+    cuuint64_t gstr[4] = {strides_bytes[0], strides_bytes[1], strides_bytes[2], strides_bytes[3]};
+    cuuint32_t bdim[5] = {box[0], box[1], box[2], box[3], box[4]};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), gdim, gstr, bdim, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID_ARG;
 }

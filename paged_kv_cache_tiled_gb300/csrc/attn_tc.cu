@@ -66,6 +66,11 @@ struct TcCfg {
     static constexpr int kNumBars = 2 * kStages + 2 * 6 + 2;
     static constexpr int kSmem = 1024 + kQBytes + kRingBytes + kNumBars * 8 + 16;
     static constexpr uint32_t kS0 = 0, kS1 = 128, kO0 = 256, kO1 = 256 + D;
+    // Paged K/V tiles hold each 8-row group's 64-channel halves side by side
+    // ([group][half][8 rows][128 B]), so that one copy lands a whole 16-token
+    // block: 8-row groups kPagedGroup bytes apart, halves 1024 bytes apart.
+    // Dense tiles hold one half after the other ([half][128 rows][128 B]).
+    static constexpr uint32_t kPagedGroup = kAtoms * 1024;
 };
 
 struct TcParams {
@@ -317,7 +322,8 @@ __device__ __noinline__ void zero_tile_rows(uint8_t* base, int z0, int z1) {
     for (int e = threadIdx.x & 31; e < n16; e += 32) {
         const int row = z0 + e / (C::kAtoms * 8);
         const int a = (e / 8) % C::kAtoms;
-        *reinterpret_cast<uint4*>(base + a * C::kAtomBytes + row * 128 + (e % 8) * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(base + (row >> 3) * C::kPagedGroup + a * 1024 + (row & 7) * 128 + (e % 8) * 16) =
+            make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -525,7 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // tile ahead, so its load latency is off the copy path
             auto load_blk = [&](int kt) -> int {
                 const int lb = kt * 8 + (lane & 7);
-                return (lane < 8 * C::kAtoms && lb * 16 < U.kv_len) ? __ldg(p.bt + (long)U.b * p.mbps + lb) : 0;
+                return (lane < 8 && lb * 16 < U.kv_len) ? __ldg(p.bt + (long)U.b * p.mbps + lb) : 0;
             };
             int blk_next = 0;
             if constexpr (MODE == MODE_PAGED) blk_next = load_blk(U.kt0);
@@ -535,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if constexpr (MODE == MODE_PAGED) {
                     const int cur = blk_next;
                     if (kt + 1 < U.n_kt) blk_next = load_blk(kt + 1);
-                    if (lane < 8 * C::kAtoms && (kt * 8 + (lane & 7)) * 16 < U.kv_len) {
+                    if (lane < 8 && (kt * 8 + lane) * 16 < U.kv_len) {
                         if (cur < 0 || cur >= p.num_blocks)
                             raise_error(p.ctx, ERR_BOUNDS_BIT);
                         else
@@ -559,9 +565,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kTileBytes);
                     __syncwarp();
                     if constexpr (MODE == MODE_PAGED) {
-                        if (lane < 8 * C::kAtoms)
-                            tma_load_4d(dst + (lane >> 3) * C::kAtomBytes + (lane & 7) * 2048, tm, &full[stage],
-                                        (lane >> 3) * 64, 0, U.hk, blk);
+                        // lane j < 8 copies the tile's j-th 16-token block
+                        if (lane < 8) {
+                            if constexpr (D == 128)
+                                tma_load_5d(dst + lane * 4096, tm, &full[stage], 0, 0, 0, 0, blk * p.Hkv + U.hk);
+                            else
+                                tma_load_4d(dst + lane * 2048, tm, &full[stage], 0, 0, U.hk, blk);
+                        }
                     } else {
                         if (lane == 0) {
 #pragma unroll
@@ -617,22 +627,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // The start-address field of a descriptor is (address >> 4) in 14 bits;
         // shared addresses stay below 256 KB, so advancing a descriptor by a byte
         // offset is adding offset >> 4.
+        // K/V tile layout: 8-row groups kv_sbo bytes apart, 64-channel halves kv_half apart
+        constexpr uint32_t kv_sbo = MODE == MODE_PAGED ? C::kPagedGroup : 1024;
+        constexpr uint32_t kv_half = MODE == MODE_PAGED ? 1024 : C::kAtomBytes;
         auto issue_qk = [&](int s, int kidx) {
-            const uint64_t kd = smem_desc_sw128(ring_addr + (kidx % S) * C::kTileBytes, 16, 1024);
+            const uint64_t kd = smem_desc_sw128(ring_addr + (kidx % S) * C::kTileBytes, 16, kv_sbo);
             const uint64_t qd = smem_desc_sw128(q_addr + s * C::kTileBytes, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * C::kAtomBytes + (kk & 3) * 32) >> 4;
-                umma_ss(tbase + s_col(s), qd + off, kd + off, kIdescQK, kk > 0);
+                const uint32_t qoff = ((kk >> 2) * C::kAtomBytes + (kk & 3) * 32) >> 4;
+                const uint32_t koff = ((kk >> 2) * kv_half + (kk & 3) * 32) >> 4;
+                umma_ss(tbase + s_col(s), qd + qoff, kd + koff, kIdescQK, kk > 0);
             }
         };
         // O_s += P_s V over keys [64h, 64h+64) of the tile
         auto issue_pv_half = [&](int s, int vidx, int h, bool acc_first) {
-            const uint64_t vd = smem_desc_sw128(ring_addr + (vidx % S) * C::kTileBytes, C::kAtomBytes, 1024);
+            const uint64_t vd = smem_desc_sw128(ring_addr + (vidx % S) * C::kTileBytes, kv_half, kv_sbo);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
-                const int kk = 4 * h + k4;
-                umma_ts(tbase + o_col(s), tbase + s_col(s) + kk * 8, vd + (uint32_t)(kk * 2048 >> 4), kIdescPV,
+                const int kk = 4 * h + k4;  // keys [16 kk, 16 kk + 16): two 8-row groups
+                umma_ts(tbase + o_col(s), tbase + s_col(s) + kk * 8, vd + (uint32_t)(kk * 2 * kv_sbo >> 4), kIdescPV,
                         (acc_first || kk > 0));
             }
         };
@@ -1189,12 +1203,22 @@ fa_status launch_paged_prefill(const void* q, const void* k_cache, const void* v
     const uint32_t qbox[4] = {64, pack ? (uint32_t)g : 1u, (uint32_t)paged_tc_slot_tokens(g), 1};
     const uint64_t dq[4] = {(uint64_t)d, (uint64_t)Hq, (uint64_t)total_q, 1};
     const uint64_t sq[3] = {(uint64_t)d * 2, (uint64_t)Hq * d * 2, (uint64_t)total_q * Hq * d * 2};
-    const uint32_t cbox[4] = {64, 16, 1, 1};
-    const uint64_t dc[4] = {(uint64_t)d, 16, (uint64_t)Hkv, (uint64_t)num_blocks};
-    const uint64_t scs[3] = {(uint64_t)d * 2, (uint64_t)16 * d * 2, (uint64_t)Hkv * 16 * d * 2};
     fa_status st = encode_tmap_bf16_4d(&tq, q, dq, sq, qbox);
-    if (st == FA_OK) st = encode_tmap_bf16_4d(&tk, k_cache, dc, scs, cbox);
-    if (st == FA_OK) st = encode_tmap_bf16_4d(&tv, v_cache, dc, scs, cbox);
+    if (d == 128) {
+        // one box per (block, kv head): 64 channels x 8 rows x 2 halves x 2 row groups,
+        // landing as [group][half][8 rows][128 B]; the last dimension is block * Hkv + head
+        const uint32_t cbox[5] = {64, 8, 2, 2, 1};
+        const uint64_t dc[5] = {64, 8, 2, 2, (uint64_t)num_blocks * Hkv};
+        const uint64_t scs[4] = {256, 128, 2048, 4096};
+        if (st == FA_OK) st = encode_tmap_bf16_5d(&tk, k_cache, dc, scs, cbox);
+        if (st == FA_OK) st = encode_tmap_bf16_5d(&tv, v_cache, dc, scs, cbox);
+    } else {
+        const uint32_t cbox[4] = {64, 16, 1, 1};
+        const uint64_t dc[4] = {(uint64_t)d, 16, (uint64_t)Hkv, (uint64_t)num_blocks};
+        const uint64_t scs[3] = {(uint64_t)d * 2, (uint64_t)16 * d * 2, (uint64_t)Hkv * 16 * d * 2};
+        if (st == FA_OK) st = encode_tmap_bf16_4d(&tk, k_cache, dc, scs, cbox);
+        if (st == FA_OK) st = encode_tmap_bf16_4d(&tv, v_cache, dc, scs, cbox);
+    }
     if (st != FA_OK) return st;
     TcParams p = base_params(0, 0, Hq, Hkv, causal, scale, out, nullptr, ctx);
     p.pack = pack ? 1 : 0;

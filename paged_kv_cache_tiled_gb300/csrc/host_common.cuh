@@ -32,6 +32,9 @@ void set_launch_count(int n);
 // cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
 fa_status encode_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4],
                               const uint64_t strides_bytes[3], const uint32_t box[4]);
+// 5-D bf16 tensor map, 128-byte swizzle (strides for dims 1..4, in bytes; any order).
+fa_status encode_tmap_bf16_5d(CUtensorMap* map, const void* base, const uint64_t dims[5], const uint64_t strides_bytes[4],
+                              const uint32_t box[5]);
 // The same for any element type and swizzle mode.
 fa_status encode_tmap_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
                          const uint32_t box[4], CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle);
