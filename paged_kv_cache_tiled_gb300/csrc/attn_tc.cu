@@ -5,10 +5,12 @@
 // the output; the score matrix never stored in device memory), for
 //   * contiguous prefill        (MODE_DENSE),
 //   * prefill with an additive mask M, classified per 128x128 tile beforehand
-//                               (MODE_MASKED),
+//     (tiles of -inf skipped; tiles of 0 read no mask; tiles of 0 and -inf
+//     that keep one run of keys per row apply that run like the causal limit;
+//     other tiles add M)        (MODE_MASKED),
 //   * chunked prefill over the paged cache, every K/V tile gathered block by
-//     block through the block table (MODE_PAGED; section "Paged Attention
-//     Kernels").
+//     block through the block table, one copy per 16-token block (MODE_PAGED;
+//     section "Paged Attention Kernels").
 //
 // CTA layout (320 threads, one CTA per SM, persistent over work units):
 //   warps 0-3   softmax warpgroup of Q slot 0, warps 4-7 of Q slot 1: thread
