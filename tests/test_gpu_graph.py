@@ -102,3 +102,30 @@ def test_replay_follows_rewritten_inputs(F):
                                         p.scale)
         assert_parity(t["out"], ref, f"graph step {s}")
     g.close()
+
+
+def test_replay_of_a_mixed_batch(F):
+    """Decode rows and long chunks in one call: the graph holds the append, the
+    decode kernel and merge, the work-list pass (captured on the library's side
+    stream, forked from and joined back to the capture stream) and the
+    tensor-core launch; replay equals the eager call bit for bit and the oracle."""
+    ctx_old = [900, 40, 2000, 0, 310, 1500]
+    q_lens = [1, 200, 2, 300, 1, 129]  # Hq/Hkv = 4: q_len <= 4 are decode rows
+    p = W.paged_case(73, ctx_old, q_lens, 8, 2, 128, num_blocks=2000)
+    t = _buffers(F, p)
+    _eager(F, p, t)
+    assert F.fa_get_error() == F.FA_OK
+    ref_out, ref_kc = t["out"].clone(), t["kc"].clone()
+    t["kc"].copy_(p.k_cache.cuda())
+    t["vc"].copy_(p.v_cache.cuda())
+    t["out"].zero_()
+    g = _graph(F, p, t)
+    assert g.kernel_count == 5           # append, decode, merge, work list, tensor-core prefill
+    assert torch.count_nonzero(t["out"]) == 0
+    g.replay()
+    assert F.fa_get_error() == F.FA_OK
+    assert torch.equal(t["out"], ref_out) and torch.equal(t["kc"], ref_kc)
+    ref, _ = oracle.paged_attention(p.q, ref_kc.cpu(), t["vc"].cpu(), p.block_table, p.ctx_lens, p.q_lens, True,
+                                    p.scale)
+    assert_parity(t["out"], ref, "mixed batch, graph replay")
+    g.close()
