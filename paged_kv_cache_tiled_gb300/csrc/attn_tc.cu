@@ -528,11 +528,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (!ok) break;
             ++qcnt;
-            // paged: lanes 0-15 each copy one 16-token block (lane & 7) of one
-            // 64-channel half; the block-table entry of the next tile is read a
-            // tile ahead, so its load latency is off the copy path
+            // paged: lane j < 8 copies the tile's j-th 16-token block (both
+            // 64-channel halves at d = 128); the block-table entries of the next
+            // tile are read a tile ahead, so their load latency is off the copy path
             auto load_blk = [&](int kt) -> int {
-                const int lb = kt * 8 + (lane & 7);
+                const int lb = kt * 8 + lane;
                 return (lane < 8 && lb * 16 < U.kv_len) ? __ldg(p.bt + (long)U.b * p.mbps + lb) : 0;
             };
             int blk_next = 0;
