@@ -121,7 +121,9 @@ fa_status fa_prefill_rows(const void* q, const void* k, const void* v, void* out
  * bit for bit.
  * Ordered on `stream` like any other call: it starts after the work already
  * queued there, and work queued after it sees out_host written; the host is
- * not synchronised.  No LSE output.  Errors: as fa_prefill, plus
+ * not synchronised.  The library-owned streams are per device and shared by
+ * every call on it (the enqueue is serialised); while a graph capture holding
+ * this call is open, another host thread must not call it on the same device.  No LSE output.  Errors: as fa_prefill, plus
  * FA_ERR_INVALID_ARG for a NULL host pointer; FA_ERR_CUDA if a copy or event
  * call fails while the pipeline is being queued (work queued before the
  * failure still runs).
@@ -277,7 +279,13 @@ fa_status fa_paged_attn_fp8(const void* q, const void* k_cache, const void* v_ca
  *                initialised
  * Sequences whose (Hq/Hkv) * q_len <= 16 take the bandwidth-bound split-KV
  * decode kernel followed by a log-sum-exp merge; longer chunks take the
- * tensor-core kernel.  Both read K/V only through the block table.
+ * tensor-core kernel.  Both read K/V only through the block table.  When a
+ * call may take both paths (Hq/Hkv <= 16 and max_q_len above the decode
+ * size), the tensor-core path's work list is built on a library-owned stream
+ * of the device, forked from and joined back to `stream` with events, beside
+ * the decode kernel: the call stays ordered on `stream` and capturable, but
+ * while a graph capture holding such a call is open, another host thread must
+ * not make such a call on the same device (that stream is part of the capture).
  */
 size_t fa_paged_attn_workspace_size(int num_seqs, int max_blocks_per_seq, int Hq, int Hkv, int d,
                                     int total_q);
