@@ -118,10 +118,14 @@ def test_repeat_calls_are_deterministic(F):
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("kind,causal", [("random", False), ("band", False), ("causal_inf", True)])
-def test_masked_parity(F, kind, causal):
+@pytest.mark.parametrize("kind,causal,d", [("random", False, 128), ("band", False, 128), ("causal_inf", True, 128),
+                                           ("band", True, 128), ("band", False, 64), ("causal_inf", False, 64)])
+def test_masked_parity(F, kind, causal, d):
+    """Band and causal masks give interval tiles (each row keeps one run of keys,
+    not always starting at the tile's first column, some rows empty), the random
+    mask general tiles; T = 520 leaves a ragged last tile row and column."""
     T = 520
-    case = W.prefill_case(31, 2, T, 4, 2, 128, causal=causal, mask_kind=kind)
+    case = W.prefill_case(31, 2, T, 4, 2, d, causal=causal, mask_kind=kind)
     lse = torch.empty(2, 4, T, device="cuda")
     out = F.fa_prefill_masked(case.q.cuda(), case.k.cuda(), case.v.cuda(), case.mask.cuda(), causal=causal,
                               scale=case.scale, lse=lse)
