@@ -11,10 +11,10 @@
 //     16-token pages; each of the grid's warps (one CTA of eight warps per SM)
 //     takes an equal contiguous range of pages, so every SM moves the same
 //     number of bytes whatever the mix of context lengths;
-//   * each warp streams its pages through a private 3-stage ring of shared
-//     memory with TMA (one 2 KB box per 64 channels of K and of V, 128-byte
-//     swizzled so the fragment loads below are bank-conflict free); the
-//     physical block id is read from the block table just before the copy;
+//   * each warp streams its pages through a private ring of shared memory
+//     with TMA (one 2 KB box per 64 channels of K and of V, 128-byte swizzled
+//     so the fragment loads below are bank-conflict free); the physical block
+//     id is read from the block table just before the copy;
 //   * all Hq/Hkv query heads of the kv head (times the chunk's query tokens,
 //     at most 16 rows) share each K/V load: they form the M dimension of
 //     m16n8k16 warp MMAs, so K and V are read from HBM exactly once;
@@ -22,12 +22,15 @@
 //     base-2 exponentials, scale * log2(e) folded into the scores);
 //   * a segment inside one warp's range is written as final bf16 output; a
 //     segment cut by a range boundary leaves fp32 partials (unnormalised O,
-//     running max, running sum) that a second kernel merges with log-sum-exp
-//     weights.
+//     running max, running sum) in shared memory, which the CTA combines with
+//     log-sum-exp weights once its warps are done: into the final rows when
+//     the segment lies inside the CTA's range, otherwise into one partial per
+//     CTA that a second kernel merges the same way.
 // Longer chunks take the tensor-core kernel (attn_tc.cu) through a work list
 // built on the device by `paged_meta_kernel`.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "host_common.cuh"
 
@@ -47,9 +50,7 @@ __host__ __device__ inline bool is_decode_row(int q_len, int g) { return q_len >
 
 // ------------------------------------------------------------------ layout --
 constexpr int kStreamWarps = 8;      // page streams per decode CTA
-constexpr int kStreamStages = 3;     // TMA ring depth per stream
 constexpr int kMaxStreamCtas = 160;  // decode grid cap (one CTA per SM); sizes the partial slots
-constexpr int kMaxStreamWarps = kMaxStreamCtas * kStreamWarps;
 
 struct PagedWs {
     size_t q_start, work_count, work_list, part_o, part_ml, total;
@@ -57,7 +58,7 @@ struct PagedWs {
 };
 
 // Workspace: scheduling lists of the tensor-core path, then two partial slots
-// per decode stream warp (16 rows of fp32 O, plus (max, sum) per row).
+// per decode CTA (16 rows of fp32 O, plus (max, sum) per row).
 inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, int total_q) {
     (void)Hq;
     (void)Hkv;
@@ -72,9 +73,9 @@ inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, i
     w.work_list = off;
     off = align256(off + sizeof(int32_t) * 2 * (size_t)w.max_entries);
     w.part_o = off;
-    off = align256(off + sizeof(float) * (size_t)2 * kMaxStreamWarps * kDecodeRows * d);
+    off = align256(off + sizeof(float) * (size_t)2 * kMaxStreamCtas * kDecodeRows * d);
     w.part_ml = off;
-    off = align256(off + sizeof(float2) * (size_t)2 * kMaxStreamWarps * kDecodeRows);
+    off = align256(off + sizeof(float2) * (size_t)2 * kMaxStreamCtas * kDecodeRows);
     w.total = off;
     return w;
 }
@@ -82,12 +83,14 @@ inline PagedWs paged_ws_layout(int num_seqs, int mbps, int Hq, int Hkv, int d, i
 // -------------------------------------------------------------- decode -----
 // Work is balanced by pages: the decode segments (sequence, kv head) are laid
 // end to end, sequence-major, as one stream of 16-token pages; warp w of the
-// grid takes pages [w*P/W, (w+1)*P/W).  A segment that lies inside one warp's
-// range is finished by that warp (bf16 output); a segment cut by a range
-// boundary leaves per-warp partials (running max, row sum, unnormalised O) in
-// slot 2w (the warp's first segment) or 2w+1 (its last), and the merge kernel
-// combines them.  Every page is read once; every warp streams the same number
-// of bytes, so no SM waits on a long sequence.
+// grid takes pages [w*P/W, (w+1)*P/W), so CTA c holds pages [8c*P/W,
+// (8c+8)*P/W).  A segment that lies inside one warp's range is finished by
+// that warp (bf16 output); a segment cut by a warp's range boundary leaves
+// that warp's partial (running max, row sum, unnormalised O) in shared memory,
+// and the CTA combines the pieces of its warps: final rows for a segment inside
+// the CTA's range, else the CTA's partial in slot 2c (the CTA's first segment)
+// or 2c+1 (its last) for the merge kernel.  Every page is read once; every warp
+// streams the same number of bytes, so no SM waits on a long sequence.
 
 // Pages one kv head of sequence s contributes to the decode stream (0 when the
 // sequence takes the tensor-core path or its lengths are inconsistent).
@@ -117,16 +120,28 @@ struct StreamSplit {
     }
 };
 
-// KV8: the 8-bit (E4M3) cache; its pages are half the bytes, so the ring is
-// twice as deep to keep the same bytes in flight.
-template <int D, bool KV8 = false>
+// Shared memory of a decode CTA: each warp's TMA ring, then each warp's slot
+// for the partial of its first segment (ROWS query rows).  The ring has three
+// stages (8 KB each at d = 128, 4 KB at d = 64) except at d = 128 with slots of
+// 16 rows, which leave room for two; the 8-bit (E4M3) cache's pages are half
+// the bytes, so its ring is twice as deep to keep the same bytes in flight.
+template <int D, bool KV8, int ROWS>
 struct StreamSmem {
     static constexpr int kPage = kBS * D * (KV8 ? 1 : 2);  // bytes of one K (or V) page
     static constexpr int kStage = 2 * kPage;              // K page + V page
-    static constexpr int kStages = KV8 ? 2 * kStreamStages : kStreamStages;
+    static constexpr int kStages = (KV8 ? 2 : 1) * (D == 128 && ROWS > 6 ? 2 : 3);
     static constexpr int kRing = kStreamWarps * kStages * kStage;
+    // a partial: ROWS rows of unnormalised O (fp32, rows kSlotRow floats
+    // apart), then (max, sum) per row
+    static constexpr int kSlotRow = D + 8;
+    static constexpr int kSlotBytes = ROWS * kSlotRow * 4 + ROWS * 8;
+    static constexpr int kSlots = kStreamWarps * kSlotBytes;
     static constexpr int kBars = kStreamWarps * kStages + 1;
-    static constexpr int kBytes = 1024 /*align slack*/ + kRing + kBars * 8 + 64;
+    static constexpr int kCutEntries = 2 * kStreamWarps;  // segments cut between the CTA's warps, at most
+    static constexpr int kBytes = 1024 /*align slack*/ + kRing + kSlots + kBars * 8 + 64 + kCutEntries * 32;
+    static_assert(kSlotBytes <= kStages * kStage, "a warp's ring holds the partial of its last segment");
+    static_assert(kSlots % 64 == 0 && kSlotBytes % 16 == 0, "slots keep 16-byte alignment");
+    static_assert((kStreamWarps * kStages * 8) % 64 == 0, "the barrier after the ring barriers is 64-byte aligned");
 };
 
 // Position of a stream cursor: sequence, kv head, block within the sequence.
@@ -146,7 +161,7 @@ struct Cursor {
 // and for P V the S tile's columns (tokens) are produced in that order by
 // loading K rows 4t+2nt+e into n-tile nt, column 2t+e.
 constexpr int kLensPerLane = 8;  // sequences per lane whose lengths are loaded in one batch
-template <int D, bool KV8 = false>
+template <int D, bool KV8, int ROWS>
 __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const uint16_t* __restrict__ q, const int32_t* __restrict__ bt,
@@ -157,13 +172,17 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     // the merge kernel that follows may be scheduled now; it waits for this
     // grid's completion before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    using L = StreamSmem<D, KV8>;
+    using L = StreamSmem<D, KV8, ROWS>;
     constexpr int kStreamStages = L::kStages;  // ring depth of this variant
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kRing);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kRing + L::kSlots);
     uint64_t* never = bars + kStreamWarps * kStreamStages;  // nothing arrives on it (time-out test hook)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(never + 1);
+    int* cut_count = const_cast<int*>(abort_flag) + 1;  // entries in cut_table
+    // 2 int4 per entry, see the end; `never` is 64-byte aligned (the ring, the
+    // slots and the barriers before it are multiples of 64 bytes), so this is 16
+    int4* cut_table = reinterpret_cast<int4*>(never + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = Hq / Hkv;
@@ -174,6 +193,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
         tma_prefetch_desc(&tm_v);
         for (int i = 0; i < L::kBars; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
+        *cut_count = 0;
         mbar_fence_init();
     }
     {
@@ -239,7 +259,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     const StreamSplit split(P, W);
     const long long b0 = split.begin(gw), b1 = split.begin(gw + 1);
     const int n_pages = (int)(b1 - b0);
-    if (n_pages <= 0) return;  // no CTA-wide synchronisation below
+    if (n_pages <= 0) return;  // not among the warps of the CTA barrier at the end
     // the lane whose sequences hold page b0 walks them (lengths are L1 hits now)
     Cursor start;
     {
@@ -273,6 +293,11 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
 
     uint8_t* ring = smem + warp * kStreamStages * L::kStage;
     uint64_t* wbar = bars + warp * kStreamStages;
+    // Partials of segments cut by a range boundary stay in shared memory:
+    // the first segment's in this warp's slot, the last one's (when it is
+    // another segment) in this warp's ring, free once its last page is read.
+    float* slot_first = reinterpret_cast<float*>(smem + L::kRing + warp * L::kSlotBytes);
+    float* slot_last = reinterpret_cast<float*>(ring);
     // advances a cursor by one page; entering a new sequence skips the ones
     // with no decode pages and carries the packed query offset along
     auto advance = [&](Cursor& c) {
@@ -326,6 +351,9 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, r8 = lane & 7;
     Cursor cc = start;            // compute cursor (all lanes)
     long long seg_first = b0 - start.blk;  // global index of the current segment's first page
+    Cursor seg_last = start;               // the segment begun last, its first page and query rows
+    long long seg_last_first = seg_first;
+    int seg_last_rows = 0, first_rows = -1;  // and the first segment's query rows
     int ctx_len = 0, q_len = 0, nrows = 0, pos_r0 = 0, pos_r1 = 0;
     uint32_t qa[D / 16][4];
     float o[D / 8][4];
@@ -334,9 +362,13 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     // starts segment (cc.s, cc.hk): loads its query rows as MMA A fragments
     // (rows r = token * g + head-in-group) and resets the softmax state
     auto begin_segment = [&]() {
+        seg_last = cc;
+        seg_last_first = seg_first;
         ctx_len = __ldg(ctx_lens + cc.s);
         q_len = __ldg(q_lens + cc.s);
         nrows = g * q_len;
+        seg_last_rows = nrows;
+        if (first_rows < 0) first_rows = nrows;
         const int rr[2] = {gid, gid + 8};
         const uint16_t* qrow[2];
 #pragma unroll
@@ -373,7 +405,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
         l0 = l1 = 0.f;
     };
     // finishes the current segment: final bf16 rows when the whole segment
-    // was in this warp's range, otherwise a partial in slot 2*gw + side
+    // was in this warp's range, otherwise a partial in shared memory
     auto end_segment = [&]() {
         float la = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
         la += __shfl_xor_sync(0xffffffffu, la, 2);
@@ -395,17 +427,18 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
                         pack_bf16x2(o[n][2 * i] * inv, o[n][2 * i + 1] * inv);
             }
         } else {
-            const long slot = 2L * gw + (seg_first <= b0 ? 0 : 1);
+            // a slot holds ROWS rows: more means max_q_len was below a chunk's length
+            if (nrows > ROWS && lane == 0) raise_error(ctx, ERR_BOUNDS_BIT);
+            float* so = seg_first <= b0 ? slot_first : slot_last;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int r = rr[i];
-                if (r >= nrows) continue;
-                float* dst = part_o + (slot * kDecodeRows + r) * D;
+                if (r >= nrows || r >= ROWS) continue;
 #pragma unroll
                 for (int n = 0; n < D / 8; ++n)
-                    *reinterpret_cast<float2*>(dst + n * 8 + tig * 2) =
+                    *reinterpret_cast<float2*>(so + r * L::kSlotRow + n * 8 + tig * 2) =
                         make_float2(o[n][2 * i] * v_scale, o[n][2 * i + 1] * v_scale);
-                if (tig == 0) part_ml[slot * kDecodeRows + r] = make_float2(ml[i], ls[i]);
+                if (tig == 0) reinterpret_cast<float2*>(so + ROWS * L::kSlotRow)[r] = make_float2(ml[i], ls[i]);
             }
         }
     };
@@ -562,19 +595,134 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
         for (int i = consumed; i < issued; ++i)
             (void)mbar_wait_bounded(&wbar[i % kStreamStages], (i / kStreamStages) & 1, 1000000000ull, nullptr);
     }
+
+    // Segments cut between this CTA's warps.  The warp holding a segment's first
+    // page within the CTA's range combines the pieces of the CTA's warps, from
+    // shared memory, with log-sum-exp weights: into the final bf16 rows when the
+    // segment lies inside the CTA's range, otherwise into the CTA's partial
+    // (slot 2c for the segment holding the CTA's first page, 2c+1 for the one
+    // holding its last) for the merge kernel.  Warps without pages have left;
+    // the barrier counts the others.
+    const int cw0 = blockIdx.x * kStreamWarps;
+    long long wb[kStreamWarps + 1];  // first page of each warp of this CTA, then the CTA's end
+#pragma unroll
+    for (int w = 0; w <= kStreamWarps; ++w) wb[w] = split.begin(cw0 + w);
+    unsigned busy = 0;  // warps of this CTA with pages
+#pragma unroll
+    for (int w = 0; w < kStreamWarps; ++w) busy |= (wb[w + 1] > wb[w] ? 1u : 0u) << w;
+    const int nbusy = __popc(busy);
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * nbusy) : "memory");
+    if (*abort_flag) return;
+    const long long c0 = wb[0], c1 = wb[kStreamWarps];
+    // 1. the warp holding a cut segment's first page within the CTA lists it:
+    //    (first query row, kv head, rows, pieces) and (output kind, slot, source slot of its own piece)
+    for (int which = 0; which < 2; ++which) {
+        const Cursor X = which ? seg_last : start;
+        const long long sf = which ? seg_last_first : b0 - start.blk;
+        if (which == 1 && sf == b0 - start.blk) break;  // one segment only
+        const long long se = sf + X.nblk;
+        if (sf >= b0 && se <= b1) continue;  // finished by this warp
+        if (sf < b0 && b0 > c0) continue;    // an earlier warp of the CTA holds its first piece here
+        // pieces: this warp and the later warps of the CTA whose pages start
+        // before the segment's end (warps without pages wrote nothing)
+        const long long lim = min(se, c1);
+        unsigned mask = 0;
+#pragma unroll
+        for (int w = 0; w < kStreamWarps; ++w)
+            if (w >= warp && wb[w] < lim && ((busy >> w) & 1u)) mask |= 1u << w;
+        if (lane == 0) {
+            const int e = atomicAdd(cut_count, 1);  // < kCutEntries: at most two per warp
+            const bool final_rows = sf >= c0 && se <= c1;
+            cut_table[2 * e] = make_int4(X.q0, X.hk, min(ROWS, which ? seg_last_rows : first_rows), (int)mask);
+            cut_table[2 * e + 1] = make_int4(final_rows ? -1 : 2 * (int)blockIdx.x + (sf <= c0 ? 0 : 1), warp, which, 0);
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * nbusy) : "memory");
+    // 2. the CTA's warps share out the listed segments' rows: per row, the
+    //    pieces are combined with log-sum-exp weights into the final bf16 row
+    //    (segment inside the CTA's range) or the CTA's partial for the merge kernel
+    const int n_cut = *cut_count;
+    const int rank = __popc(busy & ((1u << warp) - 1u));
+    constexpr int kPer = D / 32;  // channels per lane
+    int e = 0, e_row0 = 0;        // entry of the current item, and its first item index
+    for (int it = rank;; it += nbusy) {
+        int4 h = make_int4(0, 0, 0, 0);
+        while (e < n_cut) {
+            h = cut_table[2 * e];
+            if (it < e_row0 + h.z) break;
+            e_row0 += h.z;
+            ++e;
+        }
+        if (e >= n_cut) break;
+        const int4 t = cut_table[2 * e + 1];
+        const int r = it - e_row0;
+        const unsigned mask = (unsigned)h.w;
+        // piece of warp w: the listing warp's own slot (first or last segment), else warp w's first-segment slot
+        auto piece = [&](int w) -> const float* {
+            if (w == t.y && t.z) return reinterpret_cast<const float*>(smem + w * kStreamStages * L::kStage);
+            return reinterpret_cast<const float*>(smem + L::kRing + w * L::kSlotBytes);
+        };
+        float2 ml[kStreamWarps];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kStreamWarps; ++w) {
+            ml[w] = ((mask >> w) & 1u) ? reinterpret_cast<const float2*>(piece(w) + ROWS * L::kSlotRow)[r]
+                                       : make_float2(-INFINITY, 0.f);
+            M = fmaxf(M, ml[w].x);
+        }
+        float lsum = 0.f, acc[kPer];
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kStreamWarps; ++w) {
+            if (!((mask >> w) & 1u)) continue;
+            const float wt = ml[w].x == -INFINITY ? 0.f : fast_exp2(ml[w].x - M);
+            lsum += wt * ml[w].y;
+            const float* src = piece(w) + r * L::kSlotRow + lane * kPer;
+            if constexpr (kPer == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(src);
+                acc[0] += wt * v.x;
+                acc[1] += wt * v.y;
+                acc[2] += wt * v.z;
+                acc[3] += wt * v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(src);
+                acc[0] += wt * v.x;
+                acc[1] += wt * v.y;
+            }
+        }
+        if (t.x < 0) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            uint16_t* dst = out + ((long)(h.x + r / g) * Hq + h.y * g + r % g) * D + lane * kPer;
+            if constexpr (kPer == 4)
+                *reinterpret_cast<uint2*>(dst) =
+                    make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+            else
+                *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        } else {
+            float* dst = part_o + ((long)t.x * kDecodeRows + r) * D + lane * kPer;
+            if constexpr (kPer == 4)
+                *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            else
+                *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+            if (lane == 0) part_ml[(long)t.x * kDecodeRows + r] = make_float2(M, lsum);
+        }
+    }
 }
 
-// Merges the partials of segments cut by stream range boundaries: for row r,
-// m = max_p m_p, l = sum_p 2^(m_p - m) l_p, O = sum_p 2^(m_p - m) O_p / l (base
-// 2, O_p unnormalised).  One CTA per (sequence, kv head) with one warp per
-// output row (as many warps as the batch's longest decode chunk has rows):
-// lane j owns channels 4j..4j+3 and piece j's statistics.  The CTAs are small
-// enough to be resident beside the decode kernel's, so the programmatic
-// launch lets them compute their offsets while it runs; they read partials
-// only after griddepcontrol.wait.
+// Merges the partials of segments cut by the decode CTAs' range boundaries (one
+// piece per CTA, the CTA having combined its warps' pieces already): for row
+// r, m = max_p m_p, l = sum_p 2^(m_p - m) l_p, O = sum_p 2^(m_p - m) O_p / l
+// (base 2, O_p unnormalised).  One CTA per (sequence, kv head) with one warp
+// per output row (as many warps as the batch's longest decode chunk has rows):
+// lane j owns channels 4j..4j+3 and piece j's statistics.  The first four
+// pieces' O rows are requested together with the statistics, the rest eight
+// (then four) at a time, so a segment cut into few pieces costs one round
+// trip.  The programmatic launch lets the CTAs compute their offsets as decode
+// CTAs exit; they read partials only after griddepcontrol.wait.
 constexpr int kMergeMaxThreads = 32 * kDecodeRows;
 template <int D>
-__global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
+__global__ void __launch_bounds__(kMergeMaxThreads, 1) paged_merge_kernel(const int32_t* __restrict__ ctx_lens,
                                                                     const int32_t* __restrict__ q_lens,
                                                                     const float* part_o, const float2* part_ml,
                                                                     uint16_t* __restrict__ out, int num_seqs,
@@ -609,20 +757,20 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
     }
     const long long P = (long long)Hkv * tot;
     const long long seg_first = (long long)Hkv * pre + (long long)hk * nblk;
-    const StreamSplit split(P, W);
-    const int w_lo = split.owner(seg_first), w_hi = split.owner(seg_first + nblk - 1);
-    const int npieces = w_hi - w_lo + 1;
-    // slot of piece k: 2w, or 2w+1 when the segment starts after warp w's first
-    // page; -1 when warp w's range is empty (fewer pages than warps: it wrote nothing)
+    const StreamSplit split(P, W);  // W: the decode grid's warps
+    const int c_lo = split.owner(seg_first) / kStreamWarps, c_hi = split.owner(seg_first + nblk - 1) / kStreamWarps;
+    const int npieces = c_hi - c_lo + 1;
+    // slot of piece k: 2c, or 2c+1 when the segment starts after CTA c's first
+    // page; -1 when CTA c's range is empty (fewer pages than warps: it wrote nothing)
     auto slot_of = [&](int k) -> long {
-        const int w = w_lo + k;
-        const long long wb = split.begin(w);
-        if (split.begin(w + 1) == wb) return -1;
-        return 2L * w + (seg_first <= wb ? 0 : 1);
+        const int c = c_lo + k;
+        const long long cb = split.begin(c * kStreamWarps);
+        if (split.begin((c + 1) * kStreamWarps) == cb) return -1;
+        return 2L * c + (seg_first <= cb ? 0 : 1);
     };
     const long lane_slot = lane < npieces ? slot_of(lane) : -1;
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (w_lo == w_hi) return;  // the whole segment was finished by one warp of the decode kernel
+    if (c_lo == c_hi) return;  // the whole segment was finished inside one decode CTA
 
     constexpr int kPer = D / 32;  // channels per lane
     float acc[kPer];
@@ -633,8 +781,28 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
     // max of earlier groups rescales the accumulators
     for (int c0 = 0; c0 < npieces; c0 += 32) {
         const long myslot = c0 + lane < npieces ? (c0 == 0 ? lane_slot : slot_of(c0 + lane)) : -1;
+        const int n = min(32, npieces - c0);
         // partials are read through L2 (ld.global.cg): the decode grid wrote them
-        // while this grid was already resident, so the read-only path is not valid
+        // while this grid was already resident, so the read-only path is not valid.
+        // The first four pieces' O rows do not depend on the statistics: requested with them.
+        float v0[4][kPer];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long sj = __shfl_sync(0xffffffffu, myslot, u);
+            if (u < n && sj >= 0) {
+                const float* src = part_o + (sj * kDecodeRows + r) * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 t4 = __ldcg(reinterpret_cast<const float4*>(src));
+                    v0[u][0] = t4.x; v0[u][1] = t4.y; v0[u][2] = t4.z; v0[u][3] = t4.w;
+                } else {
+                    const float2 t2 = __ldcg(reinterpret_cast<const float2*>(src));
+                    v0[u][0] = t2.x; v0[u][1] = t2.y;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kPer; ++c) v0[u][c] = 0.f;
+            }
+        }
         const float2 ml = myslot >= 0 ? __ldcg(part_ml + myslot * kDecodeRows + r) : make_float2(-INFINITY, 0.f);
         float gm = ml.x;
 #pragma unroll
@@ -648,8 +816,13 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
         M = Mn;
         const float w = myslot >= 0 ? fast_exp2(ml.x - M) : 0.f;
         lsum += w * ml.y;
-        const int n = min(32, npieces - c0);
-        int j = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float wu = __shfl_sync(0xffffffffu, w, u);  // 0 past the group or for an empty range
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) acc[c] += wu * v0[u][c];
+        }
+        int j = 4;
         for (; j + 8 <= n; j += 8) {  // eight pieces' loads in flight at once
             float v[8][kPer];
             float wj[8];
@@ -674,13 +847,33 @@ __global__ void __launch_bounds__(kMergeMaxThreads) paged_merge_kernel(const int
 #pragma unroll
                 for (int c = 0; c < kPer; ++c) acc[c] += wj[u] * v[u][c];
         }
-        for (; j < n; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, j);
-            const long sj = __shfl_sync(0xffffffffu, myslot, j);
-            if (sj < 0) continue;  // uniform across the warp
-            const float* src = part_o + (sj * kDecodeRows + r) * D + lane * kPer;
+        for (; j < n; j += 4) {  // the rest, four pieces' loads in flight at once
+            float v[4][kPer];
+            float wj[4];
 #pragma unroll
-            for (int c = 0; c < kPer; ++c) acc[c] += wj * __ldcg(src + c);
+            for (int u = 0; u < 4; ++u) {
+                const int k = j + u;
+                wj[u] = __shfl_sync(0xffffffffu, w, k & 31);
+                const long sj = __shfl_sync(0xffffffffu, myslot, k & 31);
+                if (k < n && sj >= 0) {
+                    const float* src = part_o + (sj * kDecodeRows + r) * D + lane * kPer;
+                    if constexpr (kPer == 4) {
+                        const float4 t4 = __ldcg(reinterpret_cast<const float4*>(src));
+                        v[u][0] = t4.x; v[u][1] = t4.y; v[u][2] = t4.z; v[u][3] = t4.w;
+                    } else {
+                        const float2 t2 = __ldcg(reinterpret_cast<const float2*>(src));
+                        v[u][0] = t2.x; v[u][1] = t2.y;
+                    }
+                } else {
+                    wj[u] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kPer; ++c) v[u][c] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < kPer; ++c) acc[c] += wj[u] * v[u][c];
         }
     }
 #pragma unroll
@@ -836,17 +1029,24 @@ static fa_status launch_decode(const void* q, const void* k_cache, const void* v
         if (st != FA_OK) return st;
         if ((st = encode_tmap_bf16_4d(&tv, v_cache, dims, strides, box)) != FA_OK) return st;
     }
-    using L = StreamSmem<D, KV8>;
-    if ((st = raise_dynamic_smem(reinterpret_cast<const void*>(paged_decode_kernel<D, KV8>), L::kBytes)) != FA_OK)
-        return st;
     float* part_o = reinterpret_cast<float*>(ws + w.part_o);
     float2* part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
     const float scale_log2 = scale * k_scale * 1.4426950408889634f;
     const int grid = std::min(sm_count(), kMaxStreamCtas);
-    paged_decode_kernel<D, KV8><<<grid, kStreamWarps * 32, L::kBytes, s>>>(
-        tk, tv, static_cast<const uint16_t*>(q), bt, ctx_lens, q_lens, static_cast<uint16_t*>(out), part_o, part_ml,
-        num_seqs, mbps, num_blocks, Hq, Hkv, q_prefetch_rows, causal, scale_log2, v_scale, ctx);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    // partial slots of 6 rows when no decode chunk has more (then the ring keeps
+    // three stages at d = 128), else of 16
+    auto launch = [&](auto rows) -> fa_status {
+        constexpr int R = decltype(rows)::value;
+        using L = StreamSmem<D, KV8, R>;
+        const fa_status st2 = raise_dynamic_smem(reinterpret_cast<const void*>(paged_decode_kernel<D, KV8, R>), L::kBytes);
+        if (st2 != FA_OK) return st2;
+        paged_decode_kernel<D, KV8, R><<<grid, kStreamWarps * 32, L::kBytes, s>>>(
+            tk, tv, static_cast<const uint16_t*>(q), bt, ctx_lens, q_lens, static_cast<uint16_t*>(out), part_o, part_ml,
+            num_seqs, mbps, num_blocks, Hq, Hkv, q_prefetch_rows, causal, scale_log2, v_scale, ctx);
+        return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    };
+    st = merge_rows <= 6 ? launch(std::integral_constant<int, 6>{}) : launch(std::integral_constant<int, kDecodeRows>{});
+    if (st != FA_OK) return st;
     ++*launches;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_seqs, Hkv, 1);

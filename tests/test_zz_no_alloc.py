@@ -81,7 +81,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(F):
 
 def test_noalloc_rejects_problems_beyond_the_scratch_size(F):
     # the scheduling lists grow with the number of sequences and query rows
-    num_seqs, mbps, Hq, Hkv, d = 2_000_000, 64, 32, 8, 128
+    num_seqs, mbps, Hq, Hkv, d = 4_000_000, 64, 32, 8, 128
     assert F.fa_paged_attn_workspace_size(num_seqs, mbps, Hq, Hkv, d, num_seqs) > F.NOALLOC_SCRATCH_BYTES
     P = ctypes.c_void_p
     dummy = P(1 << 20)  # never dereferenced: the size check comes first
