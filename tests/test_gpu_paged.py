@@ -211,3 +211,18 @@ def test_empty_sequences_in_the_batch(F, route):
     ref, _, _ = oracle_paged(p, bits(kc), bits(vc))
     assert_parity(out, ref, f"empty sequences ({route})")
 
+
+
+def test_max_q_len_below_a_chunk_is_reported(F):
+    """max_q_len is the caller's bound on every q_len; the decode CTAs keep the
+    partials of cut segments in slots sized from it (6 rows here: Hq/Hkv = 6,
+    max_q_len = 1).  A two-token chunk (12 rows) under that bound is reported as
+    FA_ERR_BOUNDS instead of overflowing a slot, and the next call with the true
+    bound matches the oracle."""
+    p = W.paged_case(43, [3000, 2000], [1, 2], 12, 2, 128, num_blocks=400)
+    _, _, _, st = run_paged(F, p, max_q_len=1, out_guard=True)
+    assert st == F.FA_ERR_BOUNDS
+    out, kc, vc, st = run_paged(F, p, max_q_len=2, out_guard=True)
+    assert st == F.FA_OK
+    ref, _, _ = oracle_paged(p, bits(kc), bits(vc))
+    assert_parity(out, ref, "chunk of two tokens with the true bound")
