@@ -270,8 +270,11 @@ fa_status fa_paged_attn_fp8(const void* q, const void* k_cache, const void* v_ca
  *                sum(q_lens) must equal total_q
  *   out          bf16 [total_q, Hq, d], 32-byte aligned
  *   max_q_len    host-side upper bound on every q_lens[s] (total_q is always
- *                a valid bound); used only to skip launching a kernel that
- *                would find no work
+ *                a valid bound); used to skip launching a kernel that would
+ *                find no work and to size the decode kernel's partial slots
+ *                ((Hq/Hkv) * max_q_len <= 6 rows keeps its deeper ring); a
+ *                decode chunk above the bound is reported as FA_ERR_BOUNDS
+ *                (fa_get_error) and its rows are not valid
  *   block_size   must be 16
  *   scale        finite and > 0, multiplies Q K^T
  *   ws           workspace of at least fa_paged_attn_workspace_size(...) bytes
