@@ -596,13 +596,14 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
             (void)mbar_wait_bounded(&wbar[i % kStreamStages], (i / kStreamStages) & 1, 1000000000ull, nullptr);
     }
 
-    // Segments cut between this CTA's warps.  The warp holding a segment's first
-    // page within the CTA's range combines the pieces of the CTA's warps, from
-    // shared memory, with log-sum-exp weights: into the final bf16 rows when the
-    // segment lies inside the CTA's range, otherwise into the CTA's partial
-    // (slot 2c for the segment holding the CTA's first page, 2c+1 for the one
-    // holding its last) for the merge kernel.  Warps without pages have left;
-    // the barrier counts the others.
+    // Segments cut between this CTA's warps (or by the CTA's range boundaries).
+    // The warp holding a segment's first page within the CTA's range lists it;
+    // then the CTA's warps share out the listed rows and combine the pieces of
+    // the CTA's warps, from shared memory, with log-sum-exp weights: into the
+    // final bf16 rows when the segment lies inside the CTA's range, otherwise
+    // into the CTA's partial (slot 2c for the segment holding the CTA's first
+    // page, 2c+1 for the one holding its last) for the merge kernel.  Warps
+    // without pages have left; the barriers count the others.
     const int cw0 = blockIdx.x * kStreamWarps;
     long long wb[kStreamWarps + 1];  // first page of each warp of this CTA, then the CTA's end
 #pragma unroll
