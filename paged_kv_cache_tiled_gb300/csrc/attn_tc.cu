@@ -56,6 +56,12 @@ constexpr int kTcRows = 128;  // rows of a Q tile and of a KV tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
+// Paged mode hands out work units at run time: the producer takes a ticket
+// from a counter in the workspace (zeroed by the metadata kernel before every
+// launch) when it starts a unit, and passes the unit to the MMA and softmax
+// warps through a ring of kUnitSlots mailboxes.
+constexpr int kUnitSlots = 4;
+constexpr int kUnitReaders = 9;  // the MMA warp and the eight softmax warps
 
 template <int D>
 struct TcCfg {
@@ -65,8 +71,8 @@ struct TcCfg {
     static constexpr int kStages = D == 128 ? 5 : 8;
     static constexpr int kQBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kStages * kTileBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * 6 + 2;
-    static constexpr int kSmem = 1024 + kQBytes + kRingBytes + kNumBars * 8 + 16;
+    static constexpr int kNumBars = 2 * kStages + 2 * 6 + 2 + 2 * kUnitSlots;
+    static constexpr int kSmem = 1024 + kQBytes + kRingBytes + kNumBars * 8 + 16 + 4 * kUnitSlots;
     static constexpr uint32_t kS0 = 0, kS1 = 128, kO0 = 256, kO1 = 256 + D;
     // Paged K/V tiles hold each 8-row group's 64-channel halves side by side
     // ([group][half][8 rows][128 B]), so that one copy lands a whole 16-token
@@ -396,6 +402,28 @@ __device__ __noinline__ float masked_logits_row(uint32_t taddr, const float* mro
     return fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])), fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
 }
 
+// The i-th unit of this CTA as the MMA and softmax warps see it: in paged mode
+// the one the producer published in mailbox i % kUnitSlots (false if the wait
+// gave up), otherwise the static order.
+template <int MODE>
+__device__ __forceinline__ bool reader_unit(int i, int& u, const TcSched& sched, int G, int num_units,
+                                            uint64_t* ufull, uint64_t* uempty, volatile int* umbox,
+                                            unsigned long long lim_ns, volatile int* abort_flag) {
+    if constexpr (MODE == MODE_PAGED) {
+        const int k = i % kUnitSlots;
+        if (!mbar_wait_warp(&ufull[k], (i / kUnitSlots) & 1, lim_ns, abort_flag)) return false;
+        int v = 0;
+        if ((threadIdx.x & 31) == 0) {
+            v = umbox[k];
+            mbar_arrive(&uempty[k]);
+        }
+        u = __shfl_sync(0xffffffffu, v, 0);
+    } else {
+        u = cta_unit(sched, i, G, num_units);
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ kernel --
 template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -418,8 +446,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* ofull = pfull + 4;
     uint64_t* drain = ofull + 2;
     uint64_t* never = drain + 1;  // nothing arrives on it (forced time-out test hook)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+    uint64_t* ufull = never + 1;            // [kUnitSlots] paged mode: unit published in the mailbox
+    uint64_t* uempty = ufull + kUnitSlots;  // [kUnitSlots] read by every reader
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uempty + kUnitSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* umbox = abort_flag + 1;  // [kUnitSlots]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -445,6 +476,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kProducerWarp && lane == 0) {
         mbar_init(&qfull[0], 1);
         mbar_init(&qfull[1], 1);
+        for (int k = 0; k < kUnitSlots; ++k) {
+            mbar_init(&ufull[k], 1);
+            mbar_init(&uempty[k], kUnitReaders);
+        }
         mbar_fence_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -455,6 +490,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         else
             n0 = p.num_units;
         const int u0 = cta_unit(sched, 0, gridDim.x, n0);
+        if constexpr (MODE == MODE_PAGED) {  // the first unit is this CTA's own: published at once
+            umbox[0] = u0;
+            mbar_arrive(&ufull[0]);
+        }
         if (u0 >= 0) {
             const Unit U0 = decode_unit<MODE>(p, u0);
             if (unit_active<MODE>(p, U0))
@@ -504,7 +543,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // copies of every CTA.
         bool held = true;
         for (int i = 0; ok; ++i) {
-            const int u = cta_unit(sched, i, G, num_units);
+            int u;
+            if constexpr (MODE == MODE_PAGED) {
+                // after its first unit a CTA takes the next unit in the longest-first
+                // order that no CTA has taken yet, and hands it to the other warps
+                u = cta_unit(sched, 0, G, num_units);
+                if (i > 0) {
+                    int v = -1;
+                    if (lane == 0) {
+                        const int t = atomicAdd(const_cast<int32_t*>(p.work_count) + 1, 1);
+                        v = t < num_units - G ? G + t : -1;
+                    }
+                    u = __shfl_sync(0xffffffffu, v, 0);
+                    const int k = i % kUnitSlots;
+                    if (i >= kUnitSlots &&
+                        !mbar_wait_warp(&uempty[k], ((i / kUnitSlots) - 1) & 1, lim_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        umbox[k] = u;
+                        mbar_arrive(&ufull[k]);
+                    }
+                    __syncwarp();
+                }
+            } else {
+                u = cta_unit(sched, i, G, num_units);
+            }
             if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             if (!unit_active<MODE>(p, U)) continue;
@@ -668,7 +733,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
 
         for (int i = 0; ok; ++i) {
-            const int u = cta_unit(sched, i, G, num_units);
+            int u;
+            if (!reader_unit<MODE>(i, u, sched, G, num_units, ufull, uempty, umbox, lim_ns, abort_flag)) {
+                ok = false;
+                break;
+            }
             if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             if (!unit_active<MODE>(p, U)) continue;
@@ -768,7 +837,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int sc = 0, oc = 0;
         bool ok = !p.ctx.force_timeout || mbar_wait_warp(never, 0, lim_ns, abort_flag);
         for (int i = 0; ok; ++i) {
-            const int u = cta_unit(sched, i, G, num_units);
+            int u;
+            if (!reader_unit<MODE>(i, u, sched, G, num_units, ufull, uempty, umbox, lim_ns, abort_flag)) {
+                ok = false;
+                break;
+            }
             if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             // query token of this thread's row, and its head within a packed slot

@@ -962,6 +962,7 @@ __global__ void __launch_bounds__(1024) paged_meta_kernel(const int32_t* __restr
         }
         hist[nbins] = run;
         *count = run < max_entries ? run : max_entries;
+        count[1] = 0;  // the tensor-core kernel's unit tickets
     }
     __syncthreads();
     for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
