@@ -128,4 +128,10 @@ def test_replay_of_a_mixed_batch(F):
     ref, _ = oracle.paged_attention(p.q, ref_kc.cpu(), t["vc"].cpu(), p.block_table, p.ctx_lens, p.q_lens, True,
                                     p.scale)
     assert_parity(t["out"], ref, "mixed batch, graph replay")
+    # a second replay: the tensor-core kernel's unit tickets are zeroed again by
+    # the captured work-list pass, so every unit is computed once more
+    t["out"].zero_()
+    g.replay()
+    assert F.fa_get_error() == F.FA_OK
+    assert torch.equal(t["out"], ref_out)
     g.close()
