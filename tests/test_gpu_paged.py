@@ -159,8 +159,9 @@ def test_corrupt_block_table_is_reported(F):
 
 def test_decode_stream_range_boundaries(F):
     """Decode work is split into equal page ranges per warp: many tiny segments
-    fall inside one range, and one long segment spans many ranges (its partials
-    are merged); every row still matches the oracle."""
+    fall inside one range, and one long segment spans many ranges and CTAs (its
+    pieces are combined inside each CTA, then across CTAs by the merge kernel);
+    every row still matches the oracle."""
     ctx_old = [0, 1, 15, 16, 31, 12000, 2, 47, 63, 64, 300, 0, 9, 100, 4, 1]
     p = W.paged_case(46, ctx_old, [1] * len(ctx_old), 12, 2, 128, num_blocks=1200)
     out, kc, vc, st = run_paged(F, p, max_q_len=1, out_guard=True)
