@@ -424,6 +424,22 @@ __device__ __forceinline__ bool reader_unit(int i, int& u, const TcSched& sched,
     return true;
 }
 
+// Warp-uniform bounded wait that sleeps between polls (for a role with slack,
+// so that it leaves its sub-partition's issue slots to the softmax warps).
+__device__ __forceinline__ bool mbar_wait_warp_sleepy(uint64_t* bar, uint32_t parity, unsigned long long limit_ns,
+                                                      volatile int* abort) {
+    bool done = mbar_try_wait(bar, parity);
+    if (!done) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!done) {
+            if (*abort || globaltimer_ns() - t0 > limit_ns) break;
+            __nanosleep(100);
+            done = mbar_try_wait(bar, parity);
+        }
+    }
+    return __all_sync(0xffffffffu, done);
+}
+
 // ------------------------------------------------------------------ kernel --
 template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -574,7 +590,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const Unit U = decode_unit<MODE>(p, u);
             if (!unit_active<MODE>(p, U)) continue;
             for (int s = 0; s < 2 && ok && i > 0; ++s) {  // unit 0's Q tiles were requested at the start
-                if (!mbar_wait_warp(&qempty[s], (qcnt & 1) ^ 1, lim_ns, abort_flag)) {
+                if (!mbar_wait_warp_sleepy(&qempty[s], (qcnt & 1) ^ 1, lim_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -623,7 +639,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 for (int which = 0; which < 2; ++which) {  // 0: K tile, 1: V tile
                     const int stage = fill % S;
-                    if (!mbar_wait_warp(&empty[stage], ((fill / S) & 1) ^ 1, lim_ns, abort_flag)) {
+                    if (!mbar_wait_warp_sleepy(&empty[stage], ((fill / S) & 1) ^ 1, lim_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
