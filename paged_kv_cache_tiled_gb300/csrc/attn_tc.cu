@@ -757,8 +757,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (u < 0) break;
             const Unit U = decode_unit<MODE>(p, u);
             if (!unit_active<MODE>(p, U)) continue;
+            // the next unit's Q tiles take ~1 us to land: a sleeping wait leaves the
+            // sub-partition's issue slots to the softmax warps' epilogue
             for (int s = 0; s < 2; ++s)
-                if (!mbar_wait_warp(&qfull[s], ucnt & 1, lim_ns, abort_flag)) ok = false;
+                if (!mbar_wait_warp_sleepy(&qfull[s], ucnt & 1, lim_ns, abort_flag)) ok = false;
             if (!ok) break;
             ++ucnt;
             int it = 0, prev_v = -1, prev_kt = -1;
